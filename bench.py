@@ -1,0 +1,418 @@
+"""Benchmark of one Muon optimizer step on synthetic data (prints ONE JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--ns-dtype bf16|fp32]
+    python bench.py --impl reference ...   # the fp64 CPU oracle on this host's cores
+
+A step is the whole hot path over one flat buffer: momentum + orthogonalization input +
+gather + Frobenius norms, 5 Newton-Schulz iterations (15 grouped tcgen05 GEMM launches),
+then decay + scaled update + scatter.  The default workload is the Llama-3-8B matrix set
+(32 layers x {q, o, k, v, gate, up, down}, 224 matrices, 6.98e9 fp32 elements per
+buffer), whose buffers are far larger than L2, so no flush is needed between steps.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on its own GPU
+(weak scaling, no collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Muon step time (ms) and Newton-Schulz TFLOP/s + % bf16 peak at 1 GB300"
+DEFAULT_WORKLOAD = "llama3_8b_x32"
+
+
+def ns_flops(shapes, is_matrix, ns_steps):
+    """(symmetric, dense) Newton-Schulz flop counts of one step.
+
+    Per iteration and matrix (m = min, n = max of the shape): the Gram X X^T costs m^2 n
+    multiply-adds on its upper half, A A costs m^3 / 2 on its upper half, B X costs m^2 n:
+    2 flops per multiply-add gives 3 m^2 n + m^3 (symmetric) against 4 m^2 n + 2 m^3 (dense).
+    """
+    sym = dense = 0.0
+    for (r, c), f in zip(shapes, is_matrix):
+        if not f:
+            continue
+        m, n = min(r, c), max(r, c)
+        sym += ns_steps * (3.0 * m * m * n + m ** 3)
+        dense += ns_steps * (4.0 * m * m * n + 2.0 * m ** 3)
+    return sym, dense
+
+
+def elementwise_bytes(n_matrix_elems, ns_dtype):
+    """Algorithmic HBM bytes of the two streaming passes per step.
+
+    Stage 1 reads G and M and writes M (12 B) and X (2 B bf16 / 4 B fp32); stage 3 reads W
+    and O (2 / 4 B) and writes W (8 B): 24 B per element on the bf16 path."""
+    x = 2 if ns_dtype == "bf16" else 4
+    return n_matrix_elems * (12 + x), n_matrix_elems * (8 + x)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def _oracle_matrix_step_seconds(r, c, seed, ns_steps=5):
+    """Seconds the fp64 oracle takes for one full step of one r x c matrix."""
+    import numpy as np
+    from oracle import muon_ref as ref
+    rng = np.random.default_rng(seed)
+    W = rng.normal(0.0, 0.02, r * c)
+    G = rng.normal(0.0, 1e-3, r * c)
+    M = np.zeros(r * c)
+    lay = ref.flat_layout([(r, c)], 1)
+    t0 = time.perf_counter()
+    ref.muon_step(W, G, M, lay, 0.02, 0.01, 0.95, True, ns_steps)
+    return time.perf_counter() - t0
+
+
+def _shape_classes(wl):
+    """Distinct matrix costs: a matrix and its transpose share one class."""
+    classes = {}
+    for (r, c), f in zip(wl.shapes, wl.is_matrix):
+        if f:
+            key = (max(r, c), min(r, c))
+            classes[key] = classes.get(key, 0) + 1
+    return classes
+
+
+def cpu_baseline(wl, ns_steps):
+    """The oracle on one matrix of each distinct shape, extrapolated to the whole step."""
+    total = 0.0
+    spent = 0.0
+    done = []
+    for (n, m), count in sorted(_shape_classes(wl).items(), key=lambda kv: kv[0][0] * kv[0][1]):
+        t = _oracle_matrix_step_seconds(n, m, seed=n + m, ns_steps=ns_steps)
+        spent += t
+        total += count * t
+        done.append(f"{n}x{m}")
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": total * 1e3, "unit": "ms", "cores": cores, "kind": "oracle",
+            "sample": (f"fp64 numpy oracle, one full step (momentum, {ns_steps} NS iterations, "
+                       f"apply) of one matrix per distinct shape ({', '.join(done)}; a matrix "
+                       f"and its transpose share a shape), {spent:.1f} s of CPU work, "
+                       f"extrapolated to all {wl.n_matrices} matrices by shape counts"),
+            "sample_seconds": spent}
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle, as it stands, on this host's cores."""
+    from muon_optimizer_step_gb300 import inputs
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    wl = inputs.WORKLOADS[args.workload]
+    ns_steps = wl.ns_steps
+    _, dense_total = ns_flops(wl.shapes, wl.is_matrix, ns_steps)
+    # Per step: one bounded sample (the largest square-ish class that keeps a step to a few
+    # seconds), extrapolated by Newton-Schulz flops to the whole workload.
+    classes = sorted(_shape_classes(wl).items(), key=lambda kv: kv[0][0] * kv[0][1])
+    n, m = classes[0][0]
+    for (nn, mm), _ in classes:
+        if nn * mm <= 4096 * 4096:
+            n, m = nn, mm
+    _, dense_sample = ns_flops([(n, m)], [True], ns_steps)
+    scale = dense_total / dense_sample
+    for _ in range(args.warmup):
+        _oracle_matrix_step_seconds(n, m, 7, ns_steps)
+    times = [_oracle_matrix_step_seconds(n, m, 7, ns_steps) * scale for _ in range(args.steps)]
+    ms = 1e3 * statistics.mean(times)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = (f"fp64 numpy oracle, one {n}x{m} matrix step per timed step, scaled by "
+              f"Newton-Schulz flops x{scale:.1f} to the {wl.n_matrices}-matrix workload")
+    line = {"impl": "reference", "metric": METRIC, "value": ms, "unit": "ms",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "matrices": wl.n_matrices, "elements": wl.numel,
+                       "ns_steps": ns_steps},
+            "cpu_baseline": {"value": ms, "unit": "ms", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": ms, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def _mem_available_bytes():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def run_ours(args):
+    import torch
+    from muon_optimizer_step_gb300 import capi, inputs
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    wl = inputs.WORKLOADS[args.workload]
+    ns_dtype = capi.MUON_NS_BF16 if args.ns_dtype == "bf16" else capi.MUON_NS_FP32
+    ns_steps = wl.ns_steps
+    lay = capi.muon_layout_create(wl.shapes, wl.n_shards, ns_dtype, wl.is_matrix)
+    S, L, N = wl.n_shards, lay.shard_len, lay.numel
+    # One allocation per buffer; shard s is a view of [s*L, (s+1)*L), the first N elements
+    # are the unsharded flat buffer.
+    Wb = torch.zeros(S * L, dtype=torch.float32, device=dev)
+    Gb = torch.zeros(S * L, dtype=torch.float32, device=dev)
+    Mb = torch.zeros(S * L, dtype=torch.float32, device=dev)
+    inputs.device_fill_weights(wl, Wb[:N])
+    inputs.device_fill_grads(wl, Gb[:N], 0)
+    W = [Wb[s * L:(s + 1) * L] for s in range(S)]
+    G = [Gb[s * L:(s + 1) * L] for s in range(S)]
+    M = [Mb[s * L:(s + 1) * L] for s in range(S)]
+    ws = capi.workspace_tensor(lay, dev)
+    torch.cuda.synchronize()
+
+    def step_stages(evs=None):
+        if evs is not None:
+            evs[0].record()
+        capi.muon_compute_momentum_inputs(G, M, lay, ws, wl.mu, wl.nesterov)
+        if evs is not None:
+            evs[1].record()
+        capi.muon_orthogonalize_updates(lay, ws, ns_steps)
+        if evs is not None:
+            evs[2].record()
+        capi.muon_apply_local_updates(W, lay, ws, wl.lr, wl.wd, ns_steps)
+        if evs is not None:
+            evs[3].record()
+
+    for _ in range(args.warmup):
+        step_stages()
+    capi.muon_check()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    t_start.record()
+    for k in range(args.steps):
+        step_stages(evs[k])
+    t_end.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    barrier()
+    capi.muon_check()
+    total_ms = t_start.elapsed_time(t_end)
+    stage_ms = [0.0, 0.0, 0.0]
+    for e in evs:
+        for j in range(3):
+            stage_ms[j] += e[j].elapsed_time(e[j + 1])
+    stage_ms = [x / args.steps for x in stage_ms]
+    if dist is not None:
+        t = torch.tensor([total_ms] + stage_ms, device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, stage_ms = float(t[0]), [float(x) for x in t[1:]]
+    ms = total_ms / args.steps
+
+    # ------------------------------------------------------------ end to end (host buffers)
+    e2e = None
+    if not args.no_e2e:
+        need = 2 * 4 * N
+        if _mem_available_bytes() > 3 * need:
+            G_h = torch.empty(N, dtype=torch.float32, pin_memory=True)
+            W_h = torch.empty(N, dtype=torch.float32, pin_memory=True)
+            G_h.copy_(Gb[:N])
+            torch.cuda.synchronize()
+
+            def e2e_step():
+                Gb[:N].copy_(G_h, non_blocking=True)
+                capi.muon_step(W, G, M, lay, ws, wl.lr, wl.wd, wl.mu, wl.nesterov, ns_steps)
+                W_h.copy_(Wb[:N], non_blocking=True)
+
+            e2e_step()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            barrier()
+            a.record()
+            n_e2e = max(1, min(args.steps, 3))
+            for _ in range(n_e2e):
+                e2e_step()
+            b.record()
+            torch.cuda.synchronize()
+            e2e_ms = a.elapsed_time(b) / n_e2e
+            if dist is not None:
+                t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+                dist.all_reduce(t, op=dist.ReduceOp.MAX)
+                e2e_ms = float(t[0])
+            e2e = {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": 4 * N,
+                   "d2h_bytes_per_step": 4 * N,
+                   "note": "muon_step with the gradient copied in from pinned host memory and "
+                           "the updated weights copied back, every step"}
+            del G_h, W_h
+        else:
+            e2e = {"value": None, "unit": "ms", "h2d_bytes_per_step": 4 * N,
+                   "d2h_bytes_per_step": 4 * N,
+                   "note": "not measured: not enough host memory for pinned buffers"}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peaks = load_peaks()
+    sym, dense = ns_flops(wl.shapes, wl.is_matrix, ns_steps)
+    n_mat_elems = sum(r * c for (r, c), f in zip(wl.shapes, wl.is_matrix) if f)
+    b1, b3 = elementwise_bytes(n_mat_elems, args.ns_dtype)
+    ns_ms = stage_ms[1]
+    ns_tflops = sym / (ns_ms * 1e-3) / 1e12
+    ew_ms = stage_ms[0] + stage_ms[2]
+    ew_gbs = (b1 + b3) / (ew_ms * 1e-3) / 1e9
+    peak_tc = peaks["bf16_tflops_sustained"]
+    launches_per_step = (2 + 3 * ns_steps + 1) if n_mat_elems else 0
+    line = {
+        "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": args.ns_dtype,
+        "dtype_detail": "fp32 weights, momentum and update arithmetic; Newton-Schulz on "
+                        + ("bf16 tensor-core operands with fp32 accumulation"
+                           if args.ns_dtype == "bf16" else "fp32 CUDA cores"),
+        "data": "synthetic",
+        "config": {"workload": wl.name, "matrices": wl.n_matrices, "elements": N,
+                   "n_shards": wl.n_shards, "ns_steps": ns_steps, "ns_dtype": args.ns_dtype,
+                   "l2": "inputs larger than L2 (%.1f GB per fp32 buffer); no flush" % (4 * N / 1e9)},
+        "ns_ms": ns_ms, "ns_tflops": ns_tflops, "ns_tflops_dense_equiv": dense / (ns_ms * 1e-3) / 1e12,
+        "ns_flops_sym": sym, "matrices_per_s": wl.n_matrices / (ms * 1e-3),
+        "stage_ms": {"momentum_inputs": stage_ms[0], "orthogonalize": stage_ms[1],
+                     "apply": stage_ms[2]},
+        "roofline": {"bound": "tensor" if args.ns_dtype == "bf16" else "alu",
+                     "kernel": "ns_phase_tc_kernel (15 launches per step)",
+                     "achieved": ns_tflops, "peak": peak_tc, "unit": "TFLOP/s",
+                     "frac": ns_tflops / peak_tc, "traffic": None,
+                     "peak_note": "%s bf16 sustained (cuBLAS loop under the power cap)" % peaks["source"]},
+        "roofline_elementwise": {"bound": "hbm", "achieved": ew_gbs, "peak": peaks["hbm_gbs"],
+                                 "unit": "GB/s", "frac": ew_gbs / peaks["hbm_gbs"],
+                                 "bytes_per_step": b1 + b3,
+                                 "stage1_gbs": b1 / (stage_ms[0] * 1e-3) / 1e9,
+                                 "stage3_gbs": b3 / (stage_ms[2] * 1e-3) / 1e9},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, ns_steps)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--ns-dtype", choices=["bf16", "fp32"], default="bf16")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

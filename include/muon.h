@@ -1,0 +1,175 @@
+/*
+ * muon.h - C ABI of libmuon.so, a GB300 (sm_103a) implementation of the per-step
+ * update of the sharded Muon optimizer for 2-D weight matrices held in flat buffers.
+ *
+ * Sources (page title, section):
+ *   [P1] "Add initial Muon+M-FSDPv2 implementation" (Megatron-LM pull request #6425):
+ *        "What does this PR do?" (all-Flat placements; owner-based design; non-matrix
+ *        parameters computed as usual) and the "Opt step" pseudocode, steps 1-6.
+ *   [P2] "core.distributed.fsdp.src.megatron_fsdp.experimental.muon" (Megatron-Core
+ *        API docs), class FsdpMuon: step(), _step_group(), _compute_momentum_inputs(),
+ *        _orthogonalize_updates(), _apply_local_updates(), "Limitations".
+ *
+ * The pages delegate the Muon arithmetic to a base class they do not print.  This
+ * library takes the standard reading: M <- mu*M + G; orthogonalization input G + mu*M
+ * (Nesterov, with the updated M) or M; quintic Newton-Schulz with
+ * (a, b, c) = (3.4445, -4.7750, 2.0315) on X/||X||_F, transposed so rows <= cols;
+ * decoupled weight decay W*(1 - lr*wd); update W -= lr*sqrt(max(1, rows/cols))*O.
+ *
+ * Conventions shared by every entry point
+ *   - Every call returns a muon_status.  Arguments are validated before anything is
+ *     launched; on a non-OK status nothing was enqueued and muon_last_error() holds a
+ *     message (thread-local).
+ *   - Pointers named *_shards / flat_* are HOST arrays of n_shards DEVICE pointers, one
+ *     per flat shard of length L (muon_layout_shard_len).  Shard s holds flat elements
+ *     [s*L, (s+1)*L); the tail of the last shard is padding and is never read or written.
+ *     n_shards = 1 is the unsharded flat buffer.  Each shard pointer must be 16-byte
+ *     aligned.  The caller owns all device memory (parameters, gradients, momentum,
+ *     workspace); the library owns only the layout handle and small device tables.
+ *   - Work is enqueued on `stream` and the call returns without waiting.  Kernels that
+ *     wait on the GPU (mbarrier pipelines) give every wait an iteration budget; when one
+ *     runs out the kernel records MUON_ERR_TIMEOUT in a device word and exits cleanly.
+ *     muon_check() synchronises the stream and reports (and clears) that word.
+ *   - The first GPU call on a layout uploads its device tables on the current device and
+ *     the first call with a given workspace pointer encodes its TMA descriptors; both
+ *     are synchronous.  Make those first calls before any CUDA-graph capture, and keep
+ *     using the same device.  A layout must not be used from two threads at once.
+ */
+#ifndef MUON_H
+#define MUON_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MUON_ABI_VERSION 1
+#define MUON_MAX_SHARDS 128
+
+typedef enum muon_status {
+  MUON_OK = 0,
+  MUON_ERR_INVALID_ARG = 1,   /* bad shape, count, NULL pointer, out-of-range scalar   */
+  MUON_ERR_ALIGNMENT = 2,     /* a device pointer is not 16-byte (or 1024-byte) aligned */
+  MUON_ERR_CUDA = 3,          /* a CUDA runtime call failed (message has the error)    */
+  MUON_ERR_TIMEOUT = 4,       /* a device-side wait ran out of its budget              */
+  MUON_ERR_OOM = 5,           /* host or device table allocation failed                */
+  MUON_ERR_UNSUPPORTED = 6    /* no sm_103a device, or a size beyond the library limits */
+} muon_status;
+
+typedef enum muon_ns_dtype {
+  MUON_NS_BF16 = 0,  /* Newton-Schulz on tcgen05 tensor cores: bf16 operands, fp32 accumulate */
+  MUON_NS_FP32 = 1   /* Newton-Schulz in fp32 on the CUDA cores (the precision path)          */
+} muon_ns_dtype;
+
+typedef struct muon_layout muon_layout; /* opaque */
+
+/* ---------------------------------------------------------------- layout (host only)
+ * muon_layout_create: describe one flat buffer ([P1] "all-Flat placements";
+ * [P2] FsdpMuon, one FSDP buffer = one parameter group).
+ *   shapes     n_params (rows, cols) pairs, int64, in flat-buffer order.  Parameters are
+ *              packed back to back with no padding; N = sum(rows*cols).
+ *   is_matrix  n_params flags; 0 marks a non-Muon parameter (a vector, an embedding the
+ *              caller excludes) whose bytes the step never touches ([P2] "Limitations":
+ *              non-2-D parameters are skipped).  NULL means every parameter is a matrix.
+ *   n_shards   1..MUON_MAX_SHARDS equal flat shards, L = ceil(N / n_shards).
+ *   ns_dtype   a muon_ns_dtype.
+ * Matrices need rows, cols >= 1 and at most 2^31-1 elements; non-matrix parameters need
+ * rows*cols >= 0.  n_params = 0 gives an empty layout on which every step is a no-op.
+ * Pure host work: no GPU is touched.  *out receives a handle freed by muon_layout_destroy.
+ */
+muon_status muon_layout_create(const int64_t* shapes, const uint8_t* is_matrix,
+                               int32_t n_params, int32_t n_shards, int32_t ns_dtype,
+                               muon_layout** out);
+/* Frees the handle and its device tables (on the device they were uploaded to).  NULL is OK. */
+muon_status muon_layout_destroy(muon_layout* layout);
+/* N, the number of flat elements described by the layout. */
+muon_status muon_layout_numel(const muon_layout* layout, int64_t* numel);
+/* L = ceil(N / n_shards), the length in elements of every shard. */
+muon_status muon_layout_shard_len(const muon_layout* layout, int64_t* shard_len);
+/* Bytes of device workspace muon_step and friends need.  The caller allocates it (e.g. a
+ * torch uint8 tensor), 1024-byte aligned, and passes the same pointer to every call. */
+muon_status muon_layout_workspace_bytes(const muon_layout* layout, size_t* bytes);
+/* Length in elements of the fp32 "full" layout used by muon_gather_full & co: every
+ * matrix parameter, row-major, each starting at a multiple of 4 elements. */
+muon_status muon_layout_full_numel(const muon_layout* layout, int64_t* numel);
+/* offsets[i] = element offset of matrix parameter i in the full layout, -1 for a
+ * non-matrix parameter.  offsets must hold n_params entries. */
+muon_status muon_full_offsets(const muon_layout* layout, int64_t* offsets);
+
+/* ---------------------------------------------------------------- the optimizer step
+ * muon_step: one optimizer step over the whole layout ([P2] FsdpMuon.step/_step_group;
+ * [P1] "Opt step" 1-6 with the owner emulated on this GPU as indexing):
+ *   1. M <- mu*M + G and the orthogonalization input X = G + mu*M (nesterov != 0) or M,
+ *      written straight into per-matrix full matrices in the workspace (the gather);
+ *   2. per matrix, Newton-Schulz for ns_steps (0..100) iterations;
+ *   3. W <- W*(1 - lr*wd) - lr*sqrt(max(1, rows/cols))*O, read back in shard order (the
+ *      scatter).  The decay of [P2] _compute_momentum_inputs is applied here, in the same
+ *      pass as the update, since X never depends on W.
+ * flat_params and flat_momentum are updated in place; flat_grads is only read.  Momentum
+ * must be zero before the first step.  Non-matrix positions and shard padding are untouched.
+ */
+muon_status muon_step(float* const* flat_params, const float* const* flat_grads,
+                      float* const* flat_momentum, const muon_layout* layout, void* workspace,
+                      float lr, float wd, float mu, int32_t nesterov, int32_t ns_steps,
+                      cudaStream_t stream);
+
+/* The three stages of muon_step, callable one by one (same arguments, same meaning).
+ * [P2] _compute_momentum_inputs: momentum update, input build, gather, Frobenius norms. */
+muon_status muon_compute_momentum_inputs(const float* const* flat_grads,
+                                         float* const* flat_momentum,
+                                         const muon_layout* layout, void* workspace, float mu,
+                                         int32_t nesterov, cudaStream_t stream);
+/* [P2] _orthogonalize_updates: Newton-Schulz of every gathered matrix, in the workspace. */
+muon_status muon_orthogonalize_updates(const muon_layout* layout, void* workspace,
+                                       int32_t ns_steps, cudaStream_t stream);
+/* [P2] _apply_local_updates: decay + scaled update into the parameter shards (scatter).
+ * ns_steps must match the value given to muon_orthogonalize_updates. */
+muon_status muon_apply_local_updates(float* const* flat_params, const muon_layout* layout,
+                                     void* workspace, float lr, float wd, int32_t ns_steps,
+                                     cudaStream_t stream);
+
+/* ---------------------------------------------------------------- owner gather / scatter
+ * [P1] "Opt step" step 3 (gather on the owner) and step 5 (scatter from the owner) as
+ * pure index maps between the shards and the fp32 full layout.  Bit copies.
+ * muon_gather_full writes every matrix of the full layout (full: device, full_numel
+ * floats); muon_scatter_updates writes the matrix positions of the shards and nothing else. */
+muon_status muon_gather_full(const muon_layout* layout, const float* const* shards,
+                             float* full, cudaStream_t stream);
+muon_status muon_scatter_updates(const muon_layout* layout, const float* full,
+                                 float* const* shards, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- full-matrix access
+ * muon_orthogonalize_full: Newton-Schulz of caller-given full matrices (fp32 full layout,
+ * device) into full_out (same layout), through the same kernels as muon_step.  Uses (and
+ * overwrites) the workspace. */
+muon_status muon_orthogonalize_full(const muon_layout* layout, void* workspace,
+                                    const float* full_in, float* full_out, int32_t ns_steps,
+                                    cudaStream_t stream);
+/* Copy the orthogonalization input the last stage 1 wrote (as stored: bf16 or fp32,
+ * before normalisation) into full_out, widened to fp32. */
+muon_status muon_export_input(const muon_layout* layout, const void* workspace,
+                              float* full_out, cudaStream_t stream);
+/* Copy the update O of the last stage 2 (ns_steps as given there) into full_out, fp32. */
+muon_status muon_export_update(const muon_layout* layout, const void* workspace,
+                               int32_t ns_steps, float* full_out, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- status
+ * Synchronises `stream`, then reports a device-side wait timeout recorded since the last
+ * check (MUON_ERR_TIMEOUT, and clears it) or a CUDA error (MUON_ERR_CUDA). */
+muon_status muon_check(cudaStream_t stream);
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* muon_last_error(void);
+/* MUON_ABI_VERSION of the loaded library. */
+int32_t muon_abi_version(void);
+/* Self-test of the bounded-wait path: launches one block that waits on an mbarrier nobody
+ * arrives on, with a budget of budget_cycles clock cycles (1..2^40).  The wait runs out,
+ * the kernel records MUON_ERR_TIMEOUT and returns; a following muon_check reports it. */
+muon_status muon_selftest_wait_timeout(int64_t budget_cycles, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MUON_H */

@@ -1,0 +1,272 @@
+"""ctypes binding of libmuon.so: the C entry points under the same names.
+
+Only argument marshalling happens here (torch tensors -> device pointers, Python
+lists -> host pointer arrays, a torch stream -> cudaStream_t); every step of the
+optimizer runs in the library's CUDA kernels.  Importing this module loads the library
+and raises if it has not been built: there is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmuon.so")
+
+MUON_OK = 0
+MUON_ERR_INVALID_ARG = 1
+MUON_ERR_ALIGNMENT = 2
+MUON_ERR_CUDA = 3
+MUON_ERR_TIMEOUT = 4
+MUON_ERR_OOM = 5
+MUON_ERR_UNSUPPORTED = 6
+MUON_NS_BF16 = 0
+MUON_NS_FP32 = 1
+MUON_MAX_SHARDS = 128
+WORKSPACE_ALIGN = 1024
+
+_STATUS_NAMES = {0: "MUON_OK", 1: "MUON_ERR_INVALID_ARG", 2: "MUON_ERR_ALIGNMENT",
+                 3: "MUON_ERR_CUDA", 4: "MUON_ERR_TIMEOUT", 5: "MUON_ERR_OOM",
+                 6: "MUON_ERR_UNSUPPORTED"}
+
+# (name, restype, argtypes) of every entry point declared in include/muon.h.
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_PP = ctypes.POINTER(ctypes.c_void_p)
+SIGNATURES = [
+    ("muon_abi_version", _I32, []),
+    ("muon_last_error", ctypes.c_char_p, []),
+    ("muon_layout_create", _I32, [ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_uint8), _I32,
+                                  _I32, _I32, ctypes.POINTER(_P)]),
+    ("muon_layout_destroy", _I32, [_P]),
+    ("muon_layout_numel", _I32, [_P, ctypes.POINTER(_I64)]),
+    ("muon_layout_shard_len", _I32, [_P, ctypes.POINTER(_I64)]),
+    ("muon_layout_workspace_bytes", _I32, [_P, ctypes.POINTER(ctypes.c_size_t)]),
+    ("muon_layout_full_numel", _I32, [_P, ctypes.POINTER(_I64)]),
+    ("muon_full_offsets", _I32, [_P, ctypes.POINTER(_I64)]),
+    ("muon_step", _I32, [_PP, _PP, _PP, _P, _P, _F, _F, _F, _I32, _I32, _P]),
+    ("muon_compute_momentum_inputs", _I32, [_PP, _PP, _P, _P, _F, _I32, _P]),
+    ("muon_orthogonalize_updates", _I32, [_P, _P, _I32, _P]),
+    ("muon_apply_local_updates", _I32, [_PP, _P, _P, _F, _F, _I32, _P]),
+    ("muon_gather_full", _I32, [_P, _PP, _P, _P]),
+    ("muon_scatter_updates", _I32, [_P, _P, _PP, _P]),
+    ("muon_orthogonalize_full", _I32, [_P, _P, _P, _P, _I32, _P]),
+    ("muon_export_input", _I32, [_P, _P, _P, _P]),
+    ("muon_export_update", _I32, [_P, _P, _I32, _P, _P]),
+    ("muon_check", _I32, [_P]),
+    ("muon_selftest_wait_timeout", _I32, [_I64, _P]),
+]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; "
+            "g.build()'); this package has no fallback path")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, res, args in SIGNATURES:
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+class MuonError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = lib.muon_last_error().decode(errors="replace")
+        super().__init__(f"{where}: {_STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def _check(status: int, where: str):
+    if status != MUON_OK:
+        raise MuonError(status, where)
+
+
+# ------------------------------------------------------------------ marshalling helpers
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _shard_array(layout, shards, name):
+    """A host array of n_shards device pointers from a tensor or a list of tensors."""
+    if not isinstance(shards, (list, tuple)):
+        shards = [shards]
+    if len(shards) != layout.n_shards:
+        raise ValueError(f"{name}: expected {layout.n_shards} shard(s), got {len(shards)}")
+    for s in shards:
+        if isinstance(s, int):
+            continue
+        import torch
+        if s.dtype != torch.float32 or not s.is_contiguous() or s.device.type != "cuda":
+            raise ValueError(f"{name}: shards must be contiguous float32 CUDA tensors")
+        if s.numel() < layout.shard_len:
+            raise ValueError(f"{name}: shard has {s.numel()} elements, layout needs {layout.shard_len}")
+    arr = (ctypes.c_void_p * max(1, len(shards)))()
+    for i, s in enumerate(shards):
+        arr[i] = s if isinstance(s, int) else s.data_ptr()
+    return arr
+
+
+class Layout:
+    """Owns a muon_layout handle (see muon_layout_create)."""
+
+    def __init__(self, handle, shapes, is_matrix, n_shards, ns_dtype):
+        self.handle = handle
+        self.shapes = shapes
+        self.is_matrix = is_matrix
+        self.n_shards = n_shards
+        self.ns_dtype = ns_dtype
+        v = _I64()
+        _check(lib.muon_layout_numel(handle, ctypes.byref(v)), "muon_layout_numel")
+        self.numel = v.value
+        _check(lib.muon_layout_shard_len(handle, ctypes.byref(v)), "muon_layout_shard_len")
+        self.shard_len = v.value
+        _check(lib.muon_layout_full_numel(handle, ctypes.byref(v)), "muon_layout_full_numel")
+        self.full_numel = v.value
+        b = ctypes.c_size_t()
+        _check(lib.muon_layout_workspace_bytes(handle, ctypes.byref(b)),
+               "muon_layout_workspace_bytes")
+        self.workspace_bytes = b.value
+        offs = (_I64 * max(1, len(shapes)))()
+        _check(lib.muon_full_offsets(handle, offs), "muon_full_offsets")
+        self.full_offsets = [offs[i] for i in range(len(shapes))]
+
+    def close(self):
+        if self.handle:
+            lib.muon_layout_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def _as_parameter_(self):
+        return self.handle
+
+
+def muon_layout_create(shapes, n_shards=1, ns_dtype=MUON_NS_BF16, is_matrix=None) -> Layout:
+    shapes = [(int(r), int(c)) for r, c in shapes]
+    n = len(shapes)
+    flat = (_I64 * max(1, 2 * n))(*[v for rc in shapes for v in rc])
+    flags = None
+    if is_matrix is not None:
+        is_matrix = [1 if f else 0 for f in is_matrix]
+        if len(is_matrix) != n:
+            raise ValueError("is_matrix must have one flag per shape")
+        flags = (ctypes.c_uint8 * max(1, n))(*is_matrix)
+    if isinstance(ns_dtype, str):
+        ns_dtype = {"bf16": MUON_NS_BF16, "fp32": MUON_NS_FP32}[ns_dtype]
+    h = ctypes.c_void_p()
+    _check(lib.muon_layout_create(flat, flags, n, int(n_shards), int(ns_dtype), ctypes.byref(h)),
+           "muon_layout_create")
+    return Layout(h, shapes, is_matrix, int(n_shards), int(ns_dtype))
+
+
+def workspace_tensor(layout: Layout, device="cuda"):
+    """A uint8 CUDA tensor of layout.workspace_bytes whose data_ptr is 1024-byte aligned."""
+    import torch
+    raw = torch.empty(layout.workspace_bytes + WORKSPACE_ALIGN, dtype=torch.uint8, device=device)
+    off = (-raw.data_ptr()) % WORKSPACE_ALIGN
+    ws = raw[off: off + layout.workspace_bytes]
+    ws._muon_base = raw  # keep the allocation alive with the view
+    return ws
+
+
+def muon_step(flat_params, flat_grads, flat_momentum, layout, workspace, lr, wd, mu,
+              nesterov=True, ns_steps=5, stream=None):
+    _check(lib.muon_step(_shard_array(layout, flat_params, "flat_params"),
+                         _shard_array(layout, flat_grads, "flat_grads"),
+                         _shard_array(layout, flat_momentum, "flat_momentum"),
+                         layout.handle, _ptr(workspace), float(lr), float(wd), float(mu),
+                         1 if nesterov else 0, int(ns_steps), _stream_handle(stream)),
+           "muon_step")
+
+
+def muon_compute_momentum_inputs(flat_grads, flat_momentum, layout, workspace, mu,
+                                 nesterov=True, stream=None):
+    _check(lib.muon_compute_momentum_inputs(
+        _shard_array(layout, flat_grads, "flat_grads"),
+        _shard_array(layout, flat_momentum, "flat_momentum"), layout.handle, _ptr(workspace),
+        float(mu), 1 if nesterov else 0, _stream_handle(stream)), "muon_compute_momentum_inputs")
+
+
+def muon_orthogonalize_updates(layout, workspace, ns_steps=5, stream=None):
+    _check(lib.muon_orthogonalize_updates(layout.handle, _ptr(workspace), int(ns_steps),
+                                          _stream_handle(stream)), "muon_orthogonalize_updates")
+
+
+def muon_apply_local_updates(flat_params, layout, workspace, lr, wd, ns_steps=5, stream=None):
+    _check(lib.muon_apply_local_updates(_shard_array(layout, flat_params, "flat_params"),
+                                        layout.handle, _ptr(workspace), float(lr), float(wd),
+                                        int(ns_steps), _stream_handle(stream)),
+           "muon_apply_local_updates")
+
+
+def muon_gather_full(layout, shards, full, stream=None):
+    _check(lib.muon_gather_full(layout.handle, _shard_array(layout, shards, "shards"), _ptr(full),
+                                _stream_handle(stream)), "muon_gather_full")
+
+
+def muon_scatter_updates(layout, full, shards, stream=None):
+    _check(lib.muon_scatter_updates(layout.handle, _ptr(full), _shard_array(layout, shards, "shards"),
+                                    _stream_handle(stream)), "muon_scatter_updates")
+
+
+def muon_orthogonalize_full(layout, workspace, full_in, full_out, ns_steps=5, stream=None):
+    _check(lib.muon_orthogonalize_full(layout.handle, _ptr(workspace), _ptr(full_in),
+                                       _ptr(full_out), int(ns_steps), _stream_handle(stream)),
+           "muon_orthogonalize_full")
+
+
+def muon_export_input(layout, workspace, full_out, stream=None):
+    _check(lib.muon_export_input(layout.handle, _ptr(workspace), _ptr(full_out),
+                                 _stream_handle(stream)), "muon_export_input")
+
+
+def muon_export_update(layout, workspace, ns_steps, full_out, stream=None):
+    _check(lib.muon_export_update(layout.handle, _ptr(workspace), int(ns_steps), _ptr(full_out),
+                                  _stream_handle(stream)), "muon_export_update")
+
+
+def muon_check(stream=None):
+    _check(lib.muon_check(_stream_handle(stream)), "muon_check")
+
+
+def muon_check_status(stream=None) -> int:
+    """Like muon_check but returns the status instead of raising."""
+    return lib.muon_check(_stream_handle(stream))
+
+
+def muon_selftest_wait_timeout(budget_cycles, stream=None):
+    _check(lib.muon_selftest_wait_timeout(int(budget_cycles), _stream_handle(stream)),
+           "muon_selftest_wait_timeout")
+
+
+def muon_last_error() -> str:
+    return lib.muon_last_error().decode(errors="replace")
+
+
+def muon_abi_version() -> int:
+    return lib.muon_abi_version()

@@ -1,0 +1,489 @@
+// C ABI of libmuon.so: argument validation, device tables, and the launch sequence of the
+// Muon step.  The step follows FsdpMuon._step_group of the Megatron-Core API docs
+// ("core.distributed.fsdp.src.megatron_fsdp.experimental.muon"): compute momentum
+// inputs, orthogonalize on the owner, apply local updates, one flat buffer at a time on
+// the caller's CUDA stream.  With one GPU the owner is this device and the gather /
+// scatter of "Add initial Muon+M-FSDPv2 implementation" ("Opt step" steps 3 and 5) are
+// index maps fused into the first and last kernels.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/muon.h"
+#include "device_common.cuh"
+#include "kernels.h"
+
+using namespace muon;
+
+struct muon_layout {
+  Plan plan;
+  DevTables dt;
+  std::mutex mu;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+constexpr long long kDefaultBudget = 4000000000LL;  // ~2 s of SM clock per wait
+constexpr int kMaxDevices = 64;
+int* g_err_word[kMaxDevices] = {nullptr};
+std::mutex g_err_mu;
+
+muon_status fail(muon_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+muon_status ok() {
+  g_last_error.clear();
+  return MUON_OK;
+}
+
+muon_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MUON_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device word where kernels record a wait that ran out (one per device, zeroed).
+muon_status err_word(int dev, int** out) {
+  if (dev < 0 || dev >= kMaxDevices) return fail(MUON_ERR_UNSUPPORTED, "device %d out of range", dev);
+  std::lock_guard<std::mutex> g(g_err_mu);
+  if (g_err_word[dev] == nullptr) {
+    int* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
+    e = cudaMemset(p, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+    g_err_word[dev] = p;
+  }
+  *out = g_err_word[dev];
+  return MUON_OK;
+}
+
+template <typename T>
+muon_status upload(const std::vector<T>& v, T** dst) {
+  *dst = nullptr;
+  if (v.empty()) return MUON_OK;
+  cudaError_t e = cudaMalloc(dst, v.size() * sizeof(T));
+  if (e != cudaSuccess) return fail(MUON_ERR_OOM, "cudaMalloc(%zu B) for a layout table: %s",
+                                    v.size() * sizeof(T), cudaGetErrorString(e));
+  e = cudaMemcpy(*dst, v.data(), v.size() * sizeof(T), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(layout table)");
+  return MUON_OK;
+}
+
+void free_tables(DevTables* dt) {
+  if (dt->device < 0) return;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  if (cur != dt->device) cudaSetDevice(dt->device);
+  cudaFree(dt->chunks);
+  cudaFree(dt->mats);
+  for (int p = 0; p < 3; ++p) {
+    cudaFree(dt->tiles[p]);
+    cudaFree(dt->cta_begin[p]);
+  }
+  cudaFree(dt->tmaps);
+  if (cur >= 0 && cur != dt->device) cudaSetDevice(cur);
+  *dt = DevTables{};
+}
+
+// Uploads the layout's tables to the current device on first use.
+muon_status ensure_device(muon_layout* L) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DevTables& dt = L->dt;
+  if (dt.device >= 0) {
+    if (dt.device != dev)
+      return fail(MUON_ERR_UNSUPPORTED, "layout was prepared on device %d, current device is %d",
+                  dt.device, dev);
+    return MUON_OK;
+  }
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (major != 10 || minor != 3)
+    return fail(MUON_ERR_UNSUPPORTED, "libmuon is built for sm_103a; device %d is sm_%d%d", dev,
+                major, minor);
+  DevTables t;
+  t.device = dev;
+  t.n_sms = sms;
+  muon_status s;
+  if ((s = err_word(dev, &t.err)) != MUON_OK) return s;
+  if ((s = upload(L->plan.chunks, &t.chunks)) != MUON_OK) { free_tables(&t); return s; }
+  if ((s = upload(L->plan.mats, &t.mats)) != MUON_OK) { free_tables(&t); return s; }
+  const bool bf16 = L->plan.ns_dtype == MUON_NS_BF16;
+  for (int p = 0; p < 3; ++p) {
+    const TileList tl = bf16 ? plan_tiles(L->plan, p, kTcBM, kTcBN, kTcBK, sms)
+                             : plan_tiles(L->plan, p, kF32BM, kF32BN, 16, sms);
+    t.grid[p] = tl.grid;
+    if ((s = upload(tl.tiles, &t.tiles[p])) != MUON_OK) { free_tables(&t); return s; }
+    if ((s = upload(tl.cta_begin, &t.cta_begin[p])) != MUON_OK) { free_tables(&t); return s; }
+  }
+  if (bf16 && !L->plan.mats.empty()) {
+    e = cudaMalloc(&t.tmaps, L->plan.mats.size() * kMapsPerMat * sizeof(CUtensorMap));
+    if (e != cudaSuccess) { free_tables(&t); return fail(MUON_ERR_OOM, "cudaMalloc(tensor maps)"); }
+    e = prepare_tc_kernel();
+    if (e != cudaSuccess) { free_tables(&t); return cuda_fail(e, "cudaFuncSetAttribute"); }
+  }
+  dt = t;
+  return MUON_OK;
+}
+
+// Encodes the TMA descriptors for this workspace (bf16 path) when it changes.
+muon_status ensure_tmaps(muon_layout* L, const void* ws) {
+  DevTables& dt = L->dt;
+  if (L->plan.ns_dtype != MUON_NS_BF16 || L->plan.mats.empty() || dt.tmap_ws == ws)
+    return MUON_OK;
+  std::vector<CUtensorMap> maps;
+  std::string err;
+  if (!encode_tensor_maps(L->plan, ws, &maps, &err)) return fail(MUON_ERR_CUDA, "%s", err.c_str());
+  // Kernels launched with the previous descriptors may still run on other streams.
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  e = cudaMemcpy(dt.tmaps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(tensor maps)");
+  dt.tmap_ws = ws;
+  return MUON_OK;
+}
+
+muon_status check_shards(const muon_layout* L, const void* const* shards, const char* name,
+                         ShardPtrs* out) {
+  std::memset(out, 0, sizeof(*out));
+  if (shards == nullptr) return fail(MUON_ERR_INVALID_ARG, "%s is NULL", name);
+  for (int s = 0; s < L->plan.n_shards; ++s) {
+    const void* p = shards[s];
+    if (p == nullptr) {
+      if (L->plan.L > 0) return fail(MUON_ERR_INVALID_ARG, "%s[%d] is NULL", name, s);
+    } else if (reinterpret_cast<uintptr_t>(p) % 16 != 0) {
+      return fail(MUON_ERR_ALIGNMENT, "%s[%d] = %p is not 16-byte aligned", name, s, p);
+    }
+    out->p[s] = const_cast<float*>(static_cast<const float*>(p));
+  }
+  return MUON_OK;
+}
+
+muon_status check_ws(const muon_layout* L, const void* ws) {
+  if (ws == nullptr) return fail(MUON_ERR_INVALID_ARG, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % kWsAlign != 0)
+    return fail(MUON_ERR_ALIGNMENT, "workspace %p is not %lld-byte aligned", ws, (long long)kWsAlign);
+  (void)L;
+  return MUON_OK;
+}
+
+muon_status check_full(const void* p, const char* name) {
+  if (p == nullptr) return fail(MUON_ERR_INVALID_ARG, "%s is NULL", name);
+  if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
+    return fail(MUON_ERR_ALIGNMENT, "%s = %p is not 16-byte aligned", name, p);
+  return MUON_OK;
+}
+
+muon_status check_steps(int32_t ns_steps) {
+  if (ns_steps < 0 || ns_steps > 100)
+    return fail(MUON_ERR_INVALID_ARG, "ns_steps=%d outside 0..100", ns_steps);
+  return MUON_OK;
+}
+
+#define MUON_TRY(expr)                    \
+  do {                                    \
+    const muon_status s_ = (expr);        \
+    if (s_ != MUON_OK) return s_;         \
+  } while (0)
+
+#define MUON_CUDA(expr, what)                          \
+  do {                                                 \
+    const cudaError_t e_ = (expr);                     \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+// ---- the three stages (arguments already validated, tables ready) ----
+muon_status run_momentum(muon_layout* L, const ShardPtrs& g, const ShardPtrs& m, void* ws,
+                         float mu, int nesterov, cudaStream_t st) {
+  MUON_CUDA(launch_momentum_input(L->plan, L->dt, g, m, ws, mu, nesterov, st), "momentum_input");
+  MUON_CUDA(launch_norm_finalize(L->plan, L->dt, ws, st), "norm_finalize");
+  return MUON_OK;
+}
+
+muon_status run_ns(muon_layout* L, void* ws, int ns_steps, cudaStream_t st) {
+  for (int it = 0; it < ns_steps; ++it) {
+    const int x_in = it & 1;
+    const int iter0 = it == 0 ? 1 : 0;
+    for (int ph = 0; ph < 3; ++ph) {
+      const cudaError_t e = L->plan.ns_dtype == MUON_NS_BF16
+                                ? launch_ns_phase_tc(L->plan, L->dt, ws, ph, x_in, iter0,
+                                                     kDefaultBudget, st)
+                                : launch_ns_phase_f32(L->plan, L->dt, ws, ph, x_in, iter0, st);
+      if (e != cudaSuccess) return cuda_fail(e, "newton_schulz phase");
+    }
+  }
+  return MUON_OK;
+}
+
+muon_status run_apply(muon_layout* L, const ShardPtrs& w, void* ws, float lr, float wd,
+                      int ns_steps, cudaStream_t st) {
+  const float decay = (float)(1.0 - (double)lr * (double)wd);
+  MUON_CUDA(launch_apply(L->plan, L->dt, w, ws, ns_steps & 1, ns_steps == 0 ? 1 : 0, decay, lr, st),
+            "apply");
+  return MUON_OK;
+}
+
+muon_status check_scalars(float lr, float wd, float mu) {
+  if (!std::isfinite(lr) || !std::isfinite(wd) || !std::isfinite(mu))
+    return fail(MUON_ERR_INVALID_ARG, "lr, wd and mu must be finite");
+  return MUON_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t muon_abi_version(void) { return MUON_ABI_VERSION; }
+
+const char* muon_last_error(void) { return g_last_error.c_str(); }
+
+muon_status muon_layout_create(const int64_t* shapes, const uint8_t* is_matrix, int32_t n_params,
+                               int32_t n_shards, int32_t ns_dtype, muon_layout** out) {
+  if (out == nullptr) return fail(MUON_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  muon_layout* L = new (std::nothrow) muon_layout();
+  if (L == nullptr) return fail(MUON_ERR_OOM, "out of host memory");
+  std::string err;
+  try {
+    err = build_plan(shapes, is_matrix, n_params, n_shards, ns_dtype, &L->plan);
+  } catch (const std::bad_alloc&) {
+    delete L;
+    return fail(MUON_ERR_OOM, "out of host memory while planning the layout");
+  }
+  if (!err.empty()) {
+    delete L;
+    return fail(MUON_ERR_INVALID_ARG, "%s", err.c_str());
+  }
+  *out = L;
+  return ok();
+}
+
+muon_status muon_layout_destroy(muon_layout* layout) {
+  if (layout == nullptr) return ok();
+  free_tables(&layout->dt);
+  delete layout;
+  return ok();
+}
+
+muon_status muon_layout_numel(const muon_layout* layout, int64_t* numel) {
+  if (layout == nullptr || numel == nullptr) return fail(MUON_ERR_INVALID_ARG, "NULL argument");
+  *numel = layout->plan.N;
+  return ok();
+}
+
+muon_status muon_layout_shard_len(const muon_layout* layout, int64_t* shard_len) {
+  if (layout == nullptr || shard_len == nullptr) return fail(MUON_ERR_INVALID_ARG, "NULL argument");
+  *shard_len = layout->plan.L;
+  return ok();
+}
+
+muon_status muon_layout_workspace_bytes(const muon_layout* layout, size_t* bytes) {
+  if (layout == nullptr || bytes == nullptr) return fail(MUON_ERR_INVALID_ARG, "NULL argument");
+  *bytes = (size_t)layout->plan.ws_bytes;
+  return ok();
+}
+
+muon_status muon_layout_full_numel(const muon_layout* layout, int64_t* numel) {
+  if (layout == nullptr || numel == nullptr) return fail(MUON_ERR_INVALID_ARG, "NULL argument");
+  *numel = layout->plan.full_numel;
+  return ok();
+}
+
+muon_status muon_full_offsets(const muon_layout* layout, int64_t* offsets) {
+  if (layout == nullptr || (offsets == nullptr && layout->plan.n_params > 0))
+    return fail(MUON_ERR_INVALID_ARG, "NULL argument");
+  for (int32_t i = 0; i < layout->plan.n_params; ++i) offsets[i] = layout->plan.full_off[i];
+  return ok();
+}
+
+muon_status muon_compute_momentum_inputs(const float* const* flat_grads,
+                                         float* const* flat_momentum, const muon_layout* layout,
+                                         void* workspace, float mu, int32_t nesterov,
+                                         cudaStream_t stream) {
+  if (layout == nullptr) return fail(MUON_ERR_INVALID_ARG, "layout is NULL");
+  muon_layout* L = const_cast<muon_layout*>(layout);
+  ShardPtrs g, m;
+  MUON_TRY(check_shards(L, reinterpret_cast<const void* const*>(flat_grads), "flat_grads", &g));
+  MUON_TRY(check_shards(L, reinterpret_cast<const void* const*>(flat_momentum), "flat_momentum", &m));
+  MUON_TRY(check_ws(L, workspace));
+  MUON_TRY(check_scalars(0.f, 0.f, mu));
+  std::lock_guard<std::mutex> guard(L->mu);
+  MUON_TRY(ensure_device(L));
+  MUON_TRY(run_momentum(L, g, m, workspace, mu, nesterov != 0, stream));
+  return ok();
+}
+
+muon_status muon_orthogonalize_updates(const muon_layout* layout, void* workspace, int32_t ns_steps,
+                                       cudaStream_t stream) {
+  if (layout == nullptr) return fail(MUON_ERR_INVALID_ARG, "layout is NULL");
+  muon_layout* L = const_cast<muon_layout*>(layout);
+  MUON_TRY(check_ws(L, workspace));
+  MUON_TRY(check_steps(ns_steps));
+  std::lock_guard<std::mutex> guard(L->mu);
+  MUON_TRY(ensure_device(L));
+  MUON_TRY(ensure_tmaps(L, workspace));
+  MUON_TRY(run_ns(L, workspace, ns_steps, stream));
+  return ok();
+}
+
+muon_status muon_apply_local_updates(float* const* flat_params, const muon_layout* layout,
+                                     void* workspace, float lr, float wd, int32_t ns_steps,
+                                     cudaStream_t stream) {
+  if (layout == nullptr) return fail(MUON_ERR_INVALID_ARG, "layout is NULL");
+  muon_layout* L = const_cast<muon_layout*>(layout);
+  ShardPtrs w;
+  MUON_TRY(check_shards(L, reinterpret_cast<const void* const*>(flat_params), "flat_params", &w));
+  MUON_TRY(check_ws(L, workspace));
+  MUON_TRY(check_steps(ns_steps));
+  MUON_TRY(check_scalars(lr, wd, 0.f));
+  std::lock_guard<std::mutex> guard(L->mu);
+  MUON_TRY(ensure_device(L));
+  MUON_TRY(run_apply(L, w, workspace, lr, wd, ns_steps, stream));
+  return ok();
+}
+
+muon_status muon_step(float* const* flat_params, const float* const* flat_grads,
+                      float* const* flat_momentum, const muon_layout* layout, void* workspace,
+                      float lr, float wd, float mu, int32_t nesterov, int32_t ns_steps,
+                      cudaStream_t stream) {
+  if (layout == nullptr) return fail(MUON_ERR_INVALID_ARG, "layout is NULL");
+  muon_layout* L = const_cast<muon_layout*>(layout);
+  ShardPtrs w, g, m;
+  MUON_TRY(check_shards(L, reinterpret_cast<const void* const*>(flat_params), "flat_params", &w));
+  MUON_TRY(check_shards(L, reinterpret_cast<const void* const*>(flat_grads), "flat_grads", &g));
+  MUON_TRY(check_shards(L, reinterpret_cast<const void* const*>(flat_momentum), "flat_momentum", &m));
+  MUON_TRY(check_ws(L, workspace));
+  MUON_TRY(check_steps(ns_steps));
+  MUON_TRY(check_scalars(lr, wd, mu));
+  std::lock_guard<std::mutex> guard(L->mu);
+  MUON_TRY(ensure_device(L));
+  MUON_TRY(ensure_tmaps(L, workspace));
+  MUON_TRY(run_momentum(L, g, m, workspace, mu, nesterov != 0, stream));
+  MUON_TRY(run_ns(L, workspace, ns_steps, stream));
+  MUON_TRY(run_apply(L, w, workspace, lr, wd, ns_steps, stream));
+  return ok();
+}
+
+muon_status muon_gather_full(const muon_layout* layout, const float* const* shards, float* full,
+                             cudaStream_t stream) {
+  if (layout == nullptr) return fail(MUON_ERR_INVALID_ARG, "layout is NULL");
+  muon_layout* L = const_cast<muon_layout*>(layout);
+  ShardPtrs s;
+  MUON_TRY(check_shards(L, reinterpret_cast<const void* const*>(shards), "shards", &s));
+  if (L->plan.full_numel > 0) MUON_TRY(check_full(full, "full"));
+  std::lock_guard<std::mutex> guard(L->mu);
+  MUON_TRY(ensure_device(L));
+  MUON_CUDA(launch_gather(L->plan, L->dt, s, full, stream), "gather");
+  return ok();
+}
+
+muon_status muon_scatter_updates(const muon_layout* layout, const float* full, float* const* shards,
+                                 cudaStream_t stream) {
+  if (layout == nullptr) return fail(MUON_ERR_INVALID_ARG, "layout is NULL");
+  muon_layout* L = const_cast<muon_layout*>(layout);
+  ShardPtrs s;
+  MUON_TRY(check_shards(L, reinterpret_cast<const void* const*>(shards), "shards", &s));
+  if (L->plan.full_numel > 0) MUON_TRY(check_full(full, "full"));
+  std::lock_guard<std::mutex> guard(L->mu);
+  MUON_TRY(ensure_device(L));
+  MUON_CUDA(launch_scatter(L->plan, L->dt, full, s, stream), "scatter");
+  return ok();
+}
+
+muon_status muon_orthogonalize_full(const muon_layout* layout, void* workspace, const float* full_in,
+                                    float* full_out, int32_t ns_steps, cudaStream_t stream) {
+  if (layout == nullptr) return fail(MUON_ERR_INVALID_ARG, "layout is NULL");
+  muon_layout* L = const_cast<muon_layout*>(layout);
+  MUON_TRY(check_ws(L, workspace));
+  MUON_TRY(check_steps(ns_steps));
+  if (L->plan.full_numel > 0) {
+    MUON_TRY(check_full(full_in, "full_in"));
+    MUON_TRY(check_full(full_out, "full_out"));
+  }
+  std::lock_guard<std::mutex> guard(L->mu);
+  MUON_TRY(ensure_device(L));
+  MUON_TRY(ensure_tmaps(L, workspace));
+  MUON_CUDA(launch_full_input(L->plan, L->dt, full_in, workspace, stream), "full_input");
+  MUON_CUDA(launch_norm_finalize(L->plan, L->dt, workspace, stream), "norm_finalize");
+  MUON_TRY(run_ns(L, workspace, ns_steps, stream));
+  MUON_CUDA(launch_export(L->plan, L->dt, workspace, ns_steps & 1, ns_steps == 0 ? 1 : 0, full_out,
+                          stream),
+            "export");
+  return ok();
+}
+
+muon_status muon_export_input(const muon_layout* layout, const void* workspace, float* full_out,
+                              cudaStream_t stream) {
+  if (layout == nullptr) return fail(MUON_ERR_INVALID_ARG, "layout is NULL");
+  muon_layout* L = const_cast<muon_layout*>(layout);
+  MUON_TRY(check_ws(L, workspace));
+  if (L->plan.full_numel > 0) MUON_TRY(check_full(full_out, "full_out"));
+  std::lock_guard<std::mutex> guard(L->mu);
+  MUON_TRY(ensure_device(L));
+  MUON_CUDA(launch_export(L->plan, L->dt, workspace, 0, 0, full_out, stream), "export");
+  return ok();
+}
+
+muon_status muon_export_update(const muon_layout* layout, const void* workspace, int32_t ns_steps,
+                               float* full_out, cudaStream_t stream) {
+  if (layout == nullptr) return fail(MUON_ERR_INVALID_ARG, "layout is NULL");
+  muon_layout* L = const_cast<muon_layout*>(layout);
+  MUON_TRY(check_ws(L, workspace));
+  MUON_TRY(check_steps(ns_steps));
+  if (L->plan.full_numel > 0) MUON_TRY(check_full(full_out, "full_out"));
+  std::lock_guard<std::mutex> guard(L->mu);
+  MUON_TRY(ensure_device(L));
+  MUON_CUDA(launch_export(L->plan, L->dt, workspace, ns_steps & 1, ns_steps == 0 ? 1 : 0,
+                          full_out, stream),
+            "export");
+  return ok();
+}
+
+muon_status muon_check(cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int dev = -1;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int* word = nullptr;
+  MUON_TRY(err_word(dev, &word));
+  int h = 0;
+  e = cudaMemcpy(&h, word, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
+  if (h != 0) {
+    cudaMemset(word, 0, sizeof(int));
+    if (h == MUON_ERR_TIMEOUT)
+      return fail(MUON_ERR_TIMEOUT, "a device-side wait ran out of its budget and the kernel exited");
+    return fail(MUON_ERR_CUDA, "device error word %d", h);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "pending CUDA error");
+  return ok();
+}
+
+muon_status muon_selftest_wait_timeout(int64_t budget_cycles, cudaStream_t stream) {
+  if (budget_cycles < 1 || budget_cycles > ((int64_t)1 << 40))
+    return fail(MUON_ERR_INVALID_ARG, "budget_cycles outside 1..2^40");
+  int dev = -1;
+  MUON_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  int* word = nullptr;
+  MUON_TRY(err_word(dev, &word));
+  MUON_CUDA(launch_selftest_timeout(word, (long long)budget_cycles, stream), "selftest");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+// Host-side launchers of the kernels (one translation unit each) used by capi.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda.h>
+
+#include "muon_internal.h"
+
+namespace muon {
+
+struct ShardPtrs;
+
+// Device-resident tables of a layout (uploaded once per device).
+struct DevTables {
+  int device = -1;
+  int n_sms = 0;
+  ChunkDev* chunks = nullptr;
+  MatDev* mats = nullptr;
+  int* err = nullptr;           // device error word (MUON_ERR_TIMEOUT when a wait gave up)
+  TileDev* tiles[3] = {nullptr, nullptr, nullptr};
+  int32_t* cta_begin[3] = {nullptr, nullptr, nullptr};
+  int grid[3] = {0, 0, 0};
+  CUtensorMap* tmaps = nullptr; // kMapsPerMat per matrix (bf16 path)
+  const void* tmap_ws = nullptr;  // workspace the tensor maps were encoded for
+};
+
+// Stage 1: momentum, orthogonalization input into X0, per-chunk sums of squares.
+cudaError_t launch_momentum_input(const Plan& plan, const DevTables& dt, const ShardPtrs& g,
+                                  const ShardPtrs& m, void* ws, float mu, int nesterov,
+                                  cudaStream_t st);
+// Full fp32 matrices -> X0 plus per-chunk sums of squares.
+cudaError_t launch_full_input(const Plan& plan, const DevTables& dt, const float* full, void* ws,
+                              cudaStream_t st);
+// Per-matrix 1/||X||_F from the chunk sums (deterministic order).
+cudaError_t launch_norm_finalize(const Plan& plan, const DevTables& dt, void* ws,
+                                 cudaStream_t st);
+// Stage 3: W <- W*decay - lr*scale*O, O read from the final X buffer.
+cudaError_t launch_apply(const Plan& plan, const DevTables& dt, const ShardPtrs& w,
+                         const void* ws, int final_buf, int pending_norm, float decay,
+                         float lr, cudaStream_t st);
+// Owner gather / scatter between shards and the fp32 full layout.
+cudaError_t launch_gather(const Plan& plan, const DevTables& dt, const ShardPtrs& src,
+                          float* full, cudaStream_t st);
+cudaError_t launch_scatter(const Plan& plan, const DevTables& dt, const float* full,
+                           const ShardPtrs& dst, cudaStream_t st);
+// X buffer (0 or 1) -> fp32 full layout, times 1/||X|| when pending_norm.
+cudaError_t launch_export(const Plan& plan, const DevTables& dt, const void* ws, int buf,
+                          int pending_norm, float* full, cudaStream_t st);
+
+// Stage 2, bf16 path: one tcgen05 GEMM phase over every matrix.
+cudaError_t launch_ns_phase_tc(const Plan& plan, const DevTables& dt, void* ws, int phase,
+                               int x_in, int iter0, long long budget, cudaStream_t st);
+// Stage 2, fp32 path: one SIMT GEMM phase over every matrix.
+cudaError_t launch_ns_phase_f32(const Plan& plan, const DevTables& dt, void* ws, int phase,
+                                int x_in, int iter0, cudaStream_t st);
+// Encodes the bf16 path's tensor maps for workspace `ws` into host memory.
+bool encode_tensor_maps(const Plan& plan, const void* ws, std::vector<CUtensorMap>* maps,
+                        std::string* err);
+// One-block kernel that waits on an mbarrier nobody arrives on, with `budget` cycles.
+cudaError_t launch_selftest_timeout(int* err, long long budget, cudaStream_t st);
+// Prepares the tcgen05 kernel (shared-memory opt-in) on the current device.
+cudaError_t prepare_tc_kernel();
+
+}  // namespace muon

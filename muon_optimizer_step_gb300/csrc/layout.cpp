@@ -1,0 +1,194 @@
+// Host planner: where every parameter lives in the flat buffer and its shards, the
+// per-matrix full layout, the chunk table of the streaming kernels, the workspace map
+// and the per-phase tile work lists of the Newton-Schulz GEMMs.
+//
+// Flat packing follows "Add initial Muon+M-FSDPv2 implementation" ("What does this PR
+// do?": all-Flat placements): parameters back to back in the caller's order, no padding,
+// shard s of n_shards holding flat [s*L, (s+1)*L) with L = ceil(N / n_shards).  Matrix
+// parameters may straddle any number of shard edges; the gather and scatter of the
+// owner ("Opt step" steps 3 and 5) are then the index map built here.
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdio>
+#include <numeric>
+#include <queue>
+
+#include "muon_internal.h"
+
+namespace muon {
+
+namespace {
+
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+std::string fmt(const char* f, long long a, long long b = 0, long long c = 0) {
+  char buf[256];
+  std::snprintf(buf, sizeof(buf), f, a, b, c);
+  return buf;
+}
+
+}  // namespace
+
+std::string build_plan(const int64_t* shapes, const uint8_t* is_matrix, int32_t n_params,
+                       int32_t n_shards, int32_t ns_dtype, Plan* plan) {
+  if (n_params < 0) return "n_params must be >= 0";
+  if (n_params > 0 && shapes == nullptr) return "shapes is NULL";
+  if (n_shards < 1 || n_shards > 128) return fmt("n_shards=%lld outside 1..128", n_shards);
+  if (ns_dtype != 0 && ns_dtype != 1) return fmt("ns_dtype=%lld is not 0 (bf16) or 1 (fp32)", ns_dtype);
+  Plan p;
+  p.n_params = n_params;
+  p.n_shards = n_shards;
+  p.ns_dtype = ns_dtype;
+  p.rows.resize(n_params);
+  p.cols.resize(n_params);
+  p.is_matrix.resize(n_params);
+  p.flat_off.resize(n_params);
+  p.full_off.assign(n_params, -1);
+  const int64_t kMaxFlat = (int64_t)1 << 46;
+  int64_t pos = 0, full = 0;
+  for (int32_t i = 0; i < n_params; ++i) {
+    const int64_t r = shapes[2 * i], c = shapes[2 * i + 1];
+    const bool mat = is_matrix ? is_matrix[i] != 0 : true;
+    p.rows[i] = r;
+    p.cols[i] = c;
+    p.is_matrix[i] = mat ? 1 : 0;
+    if (mat) {
+      if (r < 1 || c < 1) return fmt("matrix parameter %lld has shape %lld x %lld", i, r, c);
+      if (r > INT32_MAX / c) return fmt("matrix parameter %lld (%lld x %lld) exceeds 2^31-1 elements", i, r, c);
+    } else {
+      if (r < 0 || c < 0) return fmt("parameter %lld has negative shape %lld x %lld", i, r, c);
+      if (c != 0 && r > kMaxFlat / c) return fmt("parameter %lld (%lld x %lld) is too large", i, r, c);
+    }
+    p.flat_off[i] = pos;
+    pos += r * c;
+    if (pos > kMaxFlat) return "flat buffer exceeds 2^46 elements";
+    if (mat) {
+      full = round_up(full, 4);
+      p.full_off[i] = full;
+      full += r * c;
+    }
+  }
+  p.N = pos;
+  p.L = (pos + n_shards - 1) / n_shards;
+  p.full_numel = full;
+
+  // Matrices, their workspace buffers and chunk tables.
+  const int64_t esz = ns_dtype == 0 ? 2 : 4;
+  int64_t n_mats = 0;
+  for (int32_t i = 0; i < n_params; ++i) n_mats += p.is_matrix[i];
+  int64_t n_chunks = 0;
+  for (int32_t i = 0; i < n_params; ++i) {
+    if (!p.is_matrix[i]) continue;
+    MatDev m{};
+    m.rows = (int32_t)p.rows[i];
+    m.cols = (int32_t)p.cols[i];
+    m.m = std::min(m.rows, m.cols);
+    m.n = std::max(m.rows, m.cols);
+    m.tall = m.rows > m.cols ? 1 : 0;
+    m.ldx = (int32_t)round_up(m.cols, 8);
+    m.lda = (int32_t)round_up(m.m, 8);
+    m.param = i;
+    m.full_off = p.full_off[i];
+    m.scale = (float)std::sqrt(std::max(1.0, (double)m.rows / (double)m.cols));
+    m.chunk_begin = (int64_t)p.chunks.size();
+    const int64_t numel = (int64_t)m.rows * m.cols;
+    const bool dense_x = (m.ldx == m.cols);
+    int64_t local = 0;
+    while (local < numel) {
+      const int64_t g = p.flat_off[i] + local;
+      const int64_t s = g / p.L;
+      const int64_t so = g - s * p.L;
+      int64_t len = std::min<int64_t>(kChunkElems, numel - local);
+      len = std::min<int64_t>(len, p.L - so);
+      ChunkDev ch{};
+      ch.mat = (int32_t)p.mats.size();
+      ch.shard = (int32_t)s;
+      ch.shard_off = so;
+      ch.local = local;
+      ch.len = (int32_t)len;
+      ch.vec = (so % 4 == 0 && local % 4 == 0 && m.full_off % 4 == 0 && dense_x) ? 1 : 0;
+      p.chunks.push_back(ch);
+      local += len;
+    }
+    m.chunk_end = (int64_t)p.chunks.size();
+    n_chunks = (int64_t)p.chunks.size();
+    p.mats.push_back(m);
+  }
+  (void)n_mats;
+  int64_t ws = 0;
+  p.ws_partials = ws;
+  ws += n_chunks * 4;
+  ws = round_up(ws, 16);
+  p.ws_inv_norm = ws;
+  ws += (int64_t)p.mats.size() * 4;
+  ws = round_up(ws, kWsAlign);
+  for (MatDev& m : p.mats) {
+    const int64_t xb = round_up((int64_t)m.rows * m.ldx * esz, kWsAlign);
+    const int64_t ab = round_up((int64_t)m.m * m.lda * esz, kWsAlign);
+    m.x0 = ws; ws += xb;
+    m.x1 = ws; ws += xb;
+    m.a = ws; ws += ab;
+    m.b = ws; ws += ab;
+  }
+  p.ws_bytes = std::max<int64_t>(ws, kWsAlign);
+  *plan = std::move(p);
+  return "";
+}
+
+TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_sms) {
+  struct Item { TileDev t; int64_t cost; };
+  std::vector<Item> items;
+  for (size_t mi = 0; mi < plan.mats.size(); ++mi) {
+    const MatDev& m = plan.mats[mi];
+    int M, N, K;
+    bool sym;
+    if (phase == kPhaseGram) { M = N = m.m; K = m.n; sym = true; }
+    else if (phase == kPhasePoly) { M = N = m.m; K = m.m; sym = true; }
+    else { M = m.rows; N = m.cols; K = m.m; sym = false; }
+    const int kb = (K + bk - 1) / bk;
+    for (int i0 = 0; i0 < M; i0 += bm) {
+      for (int j0 = 0; j0 < N; j0 += bn) {
+        // Symmetric outputs: only tiles that reach the upper triangle (col >= row).
+        if (sym && j0 + bn - 1 < i0) continue;
+        Item it;
+        it.t.mat = (int32_t)mi;
+        it.t.i0 = i0;
+        it.t.j0 = j0;
+        it.t.kblocks = kb;
+        it.cost = (int64_t)kb + (sym ? 3 : 2);  // k-blocks plus an epilogue allowance
+        items.push_back(it);
+      }
+    }
+  }
+  std::stable_sort(items.begin(), items.end(),
+                   [](const Item& a, const Item& b) { return a.cost > b.cost; });
+  TileList tl;
+  if (items.empty() || n_sms <= 0) {
+    tl.grid = 0;
+    tl.cta_begin.assign(1, 0);
+    return tl;
+  }
+  const int grid = (int)std::min<int64_t>((int64_t)items.size(), n_sms);
+  // LPT: each tile, most expensive first, goes to the least-loaded CTA (lowest index on ties).
+  using Slot = std::pair<int64_t, int>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int c = 0; c < grid; ++c) heap.push({0, c});
+  std::vector<std::vector<TileDev>> per(grid);
+  for (const Item& it : items) {
+    Slot s = heap.top();
+    heap.pop();
+    per[s.second].push_back(it.t);
+    heap.push({s.first + it.cost, s.second});
+  }
+  tl.grid = grid;
+  tl.cta_begin.resize(grid + 1);
+  tl.cta_begin[0] = 0;
+  for (int c = 0; c < grid; ++c) {
+    tl.cta_begin[c + 1] = tl.cta_begin[c] + (int32_t)per[c].size();
+    tl.tiles.insert(tl.tiles.end(), per[c].begin(), per[c].end());
+  }
+  return tl;
+}
+
+}  // namespace muon

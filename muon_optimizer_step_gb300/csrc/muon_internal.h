@@ -1,0 +1,101 @@
+// Internal data structures shared by the host planner (layout.cpp), the C ABI
+// (capi.cu) and the kernels.  Plain structs only, so that g++ and nvcc agree on them.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+namespace muon {
+
+// Flat elements handled by one entry of the chunk table.  A chunk never crosses a
+// matrix boundary or a shard edge, so a kernel reads it through one shard pointer.
+constexpr int kChunkElems = 32768;
+
+// Workspace alignment of every per-matrix buffer (TMA wants 16 B; SW128 tiles 1024 B).
+constexpr int64_t kWsAlign = 1024;
+
+// tcgen05 NS tile (bf16 path) and SIMT NS tile (fp32 path).
+constexpr int kTcBM = 128;
+constexpr int kTcBN = 256;
+constexpr int kTcBK = 64;
+constexpr int kF32BM = 128;
+constexpr int kF32BN = 128;
+
+// Tensor maps per matrix on the bf16 path (index = mat * kMapsPerMat + slot).
+enum MapSlot {
+  kMapX0K128 = 0, kMapX0K256 = 1, kMapX0MN = 2,
+  kMapX1K128 = 3, kMapX1K256 = 4, kMapX1MN = 5,
+  kMapAK128 = 6, kMapAK256 = 7,
+  kMapBK128 = 8, kMapBK256 = 9,
+  kMapsPerMat = 10
+};
+
+enum Phase { kPhaseGram = 0, kPhasePoly = 1, kPhaseUpdate = 2 };
+
+struct ChunkDev {          // 32 bytes
+  int32_t mat;             // matrix index (dense, over matrix parameters only)
+  int32_t shard;           // shard holding the whole chunk
+  int64_t shard_off;       // element offset inside that shard
+  int64_t local;           // row-major element index inside the matrix
+  int32_t len;             // elements in the chunk
+  int32_t vec;             // 1: shard_off, local, full offset and length allow float4
+};
+
+struct MatDev {            // 96 bytes
+  int32_t rows, cols;      // stored shape
+  int32_t m, n;            // min / max of (rows, cols)
+  int32_t tall;            // rows > cols: work on X^T (A = X^T X, X' = aX + X B)
+  int32_t ldx;             // row pitch (elements) of the X buffers
+  int32_t lda;             // row pitch (elements) of the A and B buffers (m x m)
+  int32_t param;           // index of the parameter in the caller's shapes list
+  int64_t x0, x1, a, b;    // byte offsets in the workspace
+  int64_t full_off;        // element offset in the fp32 full layout
+  int64_t chunk_begin;     // chunk table range of this matrix
+  int64_t chunk_end;
+  float scale;             // sqrt(max(1, rows/cols))
+  float pad_;
+};
+
+struct TileDev {           // 16 bytes: one output tile of one GEMM phase
+  int32_t mat;
+  int32_t i0, j0;          // first row / column of the tile in the phase's output
+  int32_t kblocks;         // ceil(K / BK): reduction length in k-blocks
+};
+
+// A per-phase work list: tiles ordered CTA by CTA, cta_begin has grid+1 entries.
+struct TileList {
+  std::vector<TileDev> tiles;
+  std::vector<int32_t> cta_begin;
+  int grid = 0;
+};
+
+// Host-side plan of one flat buffer (everything that needs no GPU).
+struct Plan {
+  int32_t n_params = 0;
+  int32_t n_shards = 1;
+  int32_t ns_dtype = 0;               // 0 bf16, 1 fp32
+  int64_t N = 0;                      // flat elements
+  int64_t L = 0;                      // shard length
+  int64_t full_numel = 0;
+  std::vector<int64_t> rows, cols;    // per parameter
+  std::vector<uint8_t> is_matrix;
+  std::vector<int64_t> flat_off;      // per parameter
+  std::vector<int64_t> full_off;      // per parameter, -1 for non-matrix
+  std::vector<MatDev> mats;           // matrix parameters with numel > 0
+  std::vector<ChunkDev> chunks;
+  // Workspace: [partials: n_chunks f32][inv_norm: n_mats f32][per-matrix buffers]
+  int64_t ws_partials = 0;
+  int64_t ws_inv_norm = 0;
+  int64_t ws_bytes = 0;
+};
+
+// Returns "" on success, else a message.  Pure host arithmetic.
+std::string build_plan(const int64_t* shapes, const uint8_t* is_matrix, int32_t n_params,
+                       int32_t n_shards, int32_t ns_dtype, Plan* plan);
+
+// Longest-processing-time assignment of a phase's tiles to `grid` CTAs (grid <= n_sms).
+TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_sms);
+
+}  // namespace muon

@@ -1,0 +1,408 @@
+// Streaming kernels of the Muon step: flat fp32 passes bound by HBM bandwidth.
+//
+//  * momentum_input: "Opt step" steps 1-3 of "Add initial Muon+M-FSDPv2 implementation"
+//    (FsdpMuon._compute_momentum_inputs in the Megatron-Core API docs): M <- mu*M + G,
+//    X = G + mu*M (Nesterov) or M, written at its row-major place in the matrix's full
+//    buffer (the owner gather, as indexing), plus a per-chunk sum of X^2 for ||X||_F.
+//  * apply: steps 5-6 (FsdpMuon._apply_local_updates): W <- W*(1 - lr*wd)
+//    - lr*sqrt(max(1, rows/cols))*O, O read from the full buffer at each flat element's
+//    place (the owner scatter, as indexing), W written in shard order.
+//  * gather / scatter / export / full_input: the same index map as bit copies.
+//
+// Every kernel walks the chunk table: a chunk lies inside one matrix and one shard, so a
+// block reads it through one shard pointer with 128-bit loads when offsets allow.
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace muon {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kBlocksPerSm = 8;
+
+__device__ __forceinline__ void store4(__nv_bfloat16* p, float a, float b, float c, float d) {
+  uint2 u;
+  u.x = pack_bf16x2(a, b);
+  u.y = pack_bf16x2(c, d);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+__device__ __forceinline__ void store4(float* p, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
+}
+__device__ __forceinline__ void store1(__nv_bfloat16* p, float a) { *p = __float2bfloat16_rn(a); }
+__device__ __forceinline__ void store1(float* p, float a) { *p = a; }
+
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+}
+__device__ __forceinline__ float4 load4(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+__device__ __forceinline__ float load1(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ float load1(const float* p) { return *p; }
+
+// Fixed-shape block sum (same order every run); the result is valid in thread 0.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float s = 0.f;
+  if (w == 0) {
+    s = (l < kThreads / 32) ? red[l] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  }
+  return s;
+}
+
+// Position of row-major element `local` of a matrix in its pitched X buffer.
+__device__ __forceinline__ int64_t x_index(const MatDev& mt, int64_t local) {
+  if (mt.ldx == mt.cols) return local;
+  const int64_t r = local / mt.cols;
+  return r * mt.ldx + (local - r * mt.cols);
+}
+
+template <typename XT>
+__global__ void __launch_bounds__(kThreads)
+momentum_input_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
+                      const MatDev* __restrict__ mats, ShardPtrs G, ShardPtrs M,
+                      uint8_t* __restrict__ ws, float* __restrict__ partials, float mu,
+                      int nesterov) {
+  __shared__ float red[32];
+  for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
+    const ChunkDev ch = chunks[ci];
+    const MatDev& mt = mats[ch.mat];
+    const float* __restrict__ g = G.p[ch.shard] + ch.shard_off;
+    float* __restrict__ m = M.p[ch.shard] + ch.shard_off;
+    XT* __restrict__ x = reinterpret_cast<XT*>(ws + mt.x0);
+    float ss = 0.f;
+    if (ch.vec) {
+      XT* xv = x + ch.local;
+      const float4* g4 = reinterpret_cast<const float4*>(g);
+      float4* m4 = reinterpret_cast<float4*>(m);
+      const int nv = ch.len >> 2;
+      int v = threadIdx.x;
+      for (; v + 3 * kThreads < nv; v += 4 * kThreads) {
+        float4 gv[4], mv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          gv[u] = __ldcs(g4 + v + u * kThreads);
+          mv[u] = __ldcs(m4 + v + u * kThreads);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float4 mn, xn;
+          mn.x = fmaf(mu, mv[u].x, gv[u].x);
+          mn.y = fmaf(mu, mv[u].y, gv[u].y);
+          mn.z = fmaf(mu, mv[u].z, gv[u].z);
+          mn.w = fmaf(mu, mv[u].w, gv[u].w);
+          if (nesterov) {
+            xn.x = fmaf(mu, mn.x, gv[u].x);
+            xn.y = fmaf(mu, mn.y, gv[u].y);
+            xn.z = fmaf(mu, mn.z, gv[u].z);
+            xn.w = fmaf(mu, mn.w, gv[u].w);
+          } else {
+            xn = mn;
+          }
+          __stcs(m4 + v + u * kThreads, mn);
+          store4(xv + 4 * (v + u * kThreads), xn.x, xn.y, xn.z, xn.w);
+          ss += xn.x * xn.x + xn.y * xn.y + xn.z * xn.z + xn.w * xn.w;
+        }
+      }
+      for (; v < nv; v += kThreads) {
+        const float4 gv = __ldcs(g4 + v);
+        const float4 mv = __ldcs(m4 + v);
+        float4 mn, xn;
+        mn.x = fmaf(mu, mv.x, gv.x);
+        mn.y = fmaf(mu, mv.y, gv.y);
+        mn.z = fmaf(mu, mv.z, gv.z);
+        mn.w = fmaf(mu, mv.w, gv.w);
+        if (nesterov) {
+          xn.x = fmaf(mu, mn.x, gv.x);
+          xn.y = fmaf(mu, mn.y, gv.y);
+          xn.z = fmaf(mu, mn.z, gv.z);
+          xn.w = fmaf(mu, mn.w, gv.w);
+        } else {
+          xn = mn;
+        }
+        __stcs(m4 + v, mn);
+        store4(xv + 4 * v, xn.x, xn.y, xn.z, xn.w);
+        ss += xn.x * xn.x + xn.y * xn.y + xn.z * xn.z + xn.w * xn.w;
+      }
+      for (int t = nv * 4 + threadIdx.x; t < ch.len; t += kThreads) {
+        const float mn = fmaf(mu, m[t], g[t]);
+        const float xn = nesterov ? fmaf(mu, mn, g[t]) : mn;
+        m[t] = mn;
+        store1(xv + t, xn);
+        ss += xn * xn;
+      }
+    } else {
+      for (int t = threadIdx.x; t < ch.len; t += kThreads) {
+        const float mn = fmaf(mu, m[t], g[t]);
+        const float xn = nesterov ? fmaf(mu, mn, g[t]) : mn;
+        m[t] = mn;
+        store1(x + x_index(mt, ch.local + t), xn);
+        ss += xn * xn;
+      }
+    }
+    const float tot = block_sum(ss, red);
+    if (threadIdx.x == 0) partials[ci] = tot;
+  }
+}
+
+template <typename XT>
+__global__ void __launch_bounds__(kThreads)
+full_input_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
+                  const MatDev* __restrict__ mats, const float* __restrict__ full,
+                  uint8_t* __restrict__ ws, float* __restrict__ partials) {
+  __shared__ float red[32];
+  for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
+    const ChunkDev ch = chunks[ci];
+    const MatDev& mt = mats[ch.mat];
+    const float* src = full + mt.full_off + ch.local;
+    XT* x = reinterpret_cast<XT*>(ws + mt.x0);
+    float ss = 0.f;
+    for (int t = threadIdx.x; t < ch.len; t += kThreads) {
+      const float v = src[t];
+      store1(x + x_index(mt, ch.local + t), v);
+      ss += v * v;
+    }
+    const float tot = block_sum(ss, red);
+    if (threadIdx.x == 0) partials[ci] = tot;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+norm_finalize_kernel(const MatDev* __restrict__ mats, int n_mats,
+                     const float* __restrict__ partials, float* __restrict__ inv_norm) {
+  __shared__ double red[kThreads];
+  for (int mi = blockIdx.x; mi < n_mats; mi += gridDim.x) {
+    const MatDev& mt = mats[mi];
+    double s = 0.0;
+    for (int64_t c = mt.chunk_begin + threadIdx.x; c < mt.chunk_end; c += kThreads)
+      s += (double)partials[c];
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int w = kThreads / 2; w > 0; w >>= 1) {
+      if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) inv_norm[mi] = red[0] > 0.0 ? (float)(1.0 / sqrt(red[0])) : 0.f;
+    __syncthreads();
+  }
+}
+
+template <typename XT>
+__global__ void __launch_bounds__(kThreads)
+apply_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
+             const MatDev* __restrict__ mats, ShardPtrs W, const uint8_t* __restrict__ ws,
+             int final_buf, const float* __restrict__ inv_norm, int pending_norm, float decay,
+             float lr) {
+  for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
+    const ChunkDev ch = chunks[ci];
+    const MatDev& mt = mats[ch.mat];
+    float lrs = lr * mt.scale;
+    if (pending_norm) lrs *= inv_norm[ch.mat];
+    const XT* __restrict__ o = reinterpret_cast<const XT*>(ws + (final_buf ? mt.x1 : mt.x0));
+    float* __restrict__ w = W.p[ch.shard] + ch.shard_off;
+    if (ch.vec) {
+      const XT* ov = o + ch.local;
+      float4* w4 = reinterpret_cast<float4*>(w);
+      const int nv = ch.len >> 2;
+      int v = threadIdx.x;
+      for (; v + 3 * kThreads < nv; v += 4 * kThreads) {
+        float4 wv[4], of[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          wv[u] = __ldcs(w4 + v + u * kThreads);
+          of[u] = load4(ov + 4 * (v + u * kThreads));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float4 r;
+          r.x = fmaf(-lrs, of[u].x, wv[u].x * decay);
+          r.y = fmaf(-lrs, of[u].y, wv[u].y * decay);
+          r.z = fmaf(-lrs, of[u].z, wv[u].z * decay);
+          r.w = fmaf(-lrs, of[u].w, wv[u].w * decay);
+          __stcs(w4 + v + u * kThreads, r);
+        }
+      }
+      for (; v < nv; v += kThreads) {
+        const float4 wv = __ldcs(w4 + v);
+        const float4 of = load4(ov + 4 * v);
+        float4 r;
+        r.x = fmaf(-lrs, of.x, wv.x * decay);
+        r.y = fmaf(-lrs, of.y, wv.y * decay);
+        r.z = fmaf(-lrs, of.z, wv.z * decay);
+        r.w = fmaf(-lrs, of.w, wv.w * decay);
+        __stcs(w4 + v, r);
+      }
+      for (int t = nv * 4 + threadIdx.x; t < ch.len; t += kThreads)
+        w[t] = fmaf(-lrs, load1(ov + t), w[t] * decay);
+    } else {
+      for (int t = threadIdx.x; t < ch.len; t += kThreads)
+        w[t] = fmaf(-lrs, load1(o + x_index(mt, ch.local + t)), w[t] * decay);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+gather_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
+              const MatDev* __restrict__ mats, ShardPtrs S, float* __restrict__ full) {
+  for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
+    const ChunkDev ch = chunks[ci];
+    const float* src = S.p[ch.shard] + ch.shard_off;
+    float* dst = full + mats[ch.mat].full_off + ch.local;
+    if (ch.vec) {
+      const int nv = ch.len >> 2;
+      for (int v = threadIdx.x; v < nv; v += kThreads)
+        reinterpret_cast<float4*>(dst)[v] = reinterpret_cast<const float4*>(src)[v];
+      for (int t = nv * 4 + threadIdx.x; t < ch.len; t += kThreads) dst[t] = src[t];
+    } else {
+      for (int t = threadIdx.x; t < ch.len; t += kThreads) dst[t] = src[t];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+scatter_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
+               const MatDev* __restrict__ mats, const float* __restrict__ full, ShardPtrs D) {
+  for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
+    const ChunkDev ch = chunks[ci];
+    float* dst = D.p[ch.shard] + ch.shard_off;
+    const float* src = full + mats[ch.mat].full_off + ch.local;
+    if (ch.vec) {
+      const int nv = ch.len >> 2;
+      for (int v = threadIdx.x; v < nv; v += kThreads)
+        reinterpret_cast<float4*>(dst)[v] = reinterpret_cast<const float4*>(src)[v];
+      for (int t = nv * 4 + threadIdx.x; t < ch.len; t += kThreads) dst[t] = src[t];
+    } else {
+      for (int t = threadIdx.x; t < ch.len; t += kThreads) dst[t] = src[t];
+    }
+  }
+}
+
+template <typename XT>
+__global__ void __launch_bounds__(kThreads)
+export_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
+              const MatDev* __restrict__ mats, const uint8_t* __restrict__ ws, int buf,
+              const float* __restrict__ inv_norm, int pending_norm, float* __restrict__ full) {
+  for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
+    const ChunkDev ch = chunks[ci];
+    const MatDev& mt = mats[ch.mat];
+    const float s = pending_norm ? inv_norm[ch.mat] : 1.f;
+    const XT* x = reinterpret_cast<const XT*>(ws + (buf ? mt.x1 : mt.x0));
+    float* dst = full + mt.full_off + ch.local;
+    for (int t = threadIdx.x; t < ch.len; t += kThreads)
+      dst[t] = load1(x + x_index(mt, ch.local + t)) * s;
+  }
+}
+
+int grid_for(const Plan& plan, const DevTables& dt) {
+  const int64_t n = (int64_t)plan.chunks.size();
+  const int64_t cap = (int64_t)dt.n_sms * kBlocksPerSm;
+  return (int)(n < cap ? n : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_momentum_input(const Plan& plan, const DevTables& dt, const ShardPtrs& g,
+                                  const ShardPtrs& m, void* ws, float mu, int nesterov,
+                                  cudaStream_t st) {
+  const int grid = grid_for(plan, dt);
+  if (grid == 0) return cudaSuccess;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* partials = reinterpret_cast<float*>(w + plan.ws_partials);
+  if (plan.ns_dtype == 0)
+    momentum_input_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, w, partials, mu, nesterov);
+  else
+    momentum_input_kernel<float><<<grid, kThreads, 0, st>>>(
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, w, partials, mu, nesterov);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_full_input(const Plan& plan, const DevTables& dt, const float* full, void* ws,
+                              cudaStream_t st) {
+  const int grid = grid_for(plan, dt);
+  if (grid == 0) return cudaSuccess;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* partials = reinterpret_cast<float*>(w + plan.ws_partials);
+  if (plan.ns_dtype == 0)
+    full_input_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, full, w, partials);
+  else
+    full_input_kernel<float><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
+                                                        dt.mats, full, w, partials);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_finalize(const Plan& plan, const DevTables& dt, void* ws,
+                                 cudaStream_t st) {
+  const int n = (int)plan.mats.size();
+  if (n == 0) return cudaSuccess;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const int grid = n < 65535 ? n : 65535;
+  norm_finalize_kernel<<<grid, kThreads, 0, st>>>(
+      dt.mats, n, reinterpret_cast<const float*>(w + plan.ws_partials),
+      reinterpret_cast<float*>(w + plan.ws_inv_norm));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_apply(const Plan& plan, const DevTables& dt, const ShardPtrs& wp,
+                         const void* ws, int final_buf, int pending_norm, float decay,
+                         float lr, cudaStream_t st) {
+  const int grid = grid_for(plan, dt);
+  if (grid == 0) return cudaSuccess;
+  const uint8_t* w = static_cast<const uint8_t*>(ws);
+  const float* inv = reinterpret_cast<const float*>(w + plan.ws_inv_norm);
+  if (plan.ns_dtype == 0)
+    apply_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, wp, w, final_buf, inv, pending_norm,
+        decay, lr);
+  else
+    apply_kernel<float><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
+                                                   dt.mats, wp, w, final_buf, inv,
+                                                   pending_norm, decay, lr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const Plan& plan, const DevTables& dt, const ShardPtrs& src,
+                          float* full, cudaStream_t st) {
+  const int grid = grid_for(plan, dt);
+  if (grid == 0) return cudaSuccess;
+  gather_kernel<<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(), dt.mats,
+                                           src, full);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const Plan& plan, const DevTables& dt, const float* full,
+                           const ShardPtrs& dst, cudaStream_t st) {
+  const int grid = grid_for(plan, dt);
+  if (grid == 0) return cudaSuccess;
+  scatter_kernel<<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(), dt.mats,
+                                            full, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_export(const Plan& plan, const DevTables& dt, const void* ws, int buf,
+                          int pending_norm, float* full, cudaStream_t st) {
+  const int grid = grid_for(plan, dt);
+  if (grid == 0) return cudaSuccess;
+  const uint8_t* w = static_cast<const uint8_t*>(ws);
+  const float* inv = reinterpret_cast<const float*>(w + plan.ws_inv_norm);
+  if (plan.ns_dtype == 0)
+    export_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, w, buf, inv, pending_norm, full);
+  else
+    export_kernel<float><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
+                                                    dt.mats, w, buf, inv, pending_norm, full);
+  return cudaGetLastError();
+}
+
+}  // namespace muon

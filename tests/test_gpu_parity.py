@@ -1,0 +1,299 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle, stage by stage.
+
+Tolerances (relative Frobenius error ||gpu - oracle|| / ||oracle||, per matrix):
+  * gather / scatter, non-matrix bytes, shard padding: bit-exact;
+  * momentum M and weights W: 1e-6 (fp32 arithmetic, one or two roundings per element);
+  * stored orthogonalization input X: 2e-3 on the bf16 path (round-to-nearest bf16 has
+    relative error <= 2^-9 per element), 1e-6 on the fp32 path;
+  * Newton-Schulz output: 2e-2 on the bf16 path, 1e-4 on the fp32 path, both against the
+    oracle run on the GPU's own stored input and against the oracle's own input.
+W is compared as oracle_apply(W_before, O_gpu) against W_gpu, so the NS tolerance does not
+leak into the 1e-6 weight check.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from oracle import muon_ref as ref  # noqa: E402
+from muon_optimizer_step_gb300 import inputs  # noqa: E402
+
+TOL_NS = {0: 2e-2, 1: 1e-4}
+TOL_X = {0: 2e-3, 1: 1e-6}
+TOL_STATE = 1e-6
+
+
+@pytest.fixture(scope="module")
+def capi():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from muon_optimizer_step_gb300 import capi as c
+    return c
+
+
+def rel(x, y):
+    x = np.asarray(x, dtype=np.float64)
+    y = np.asarray(y, dtype=np.float64)
+    d = np.linalg.norm(y)
+    return float(np.linalg.norm(x - y) / d) if d > 0 else float(np.linalg.norm(x))
+
+
+def split_shards(flat, n_shards):
+    """Plain numpy split of a flat vector into n_shards zero-padded shards of ceil(N/S)."""
+    flat = np.asarray(flat, dtype=np.float32)
+    L = -(-flat.size // n_shards)
+    padded = np.zeros(L * n_shards, dtype=np.float32)
+    padded[: flat.size] = flat
+    return [torch.from_numpy(padded[s * L:(s + 1) * L].copy()).cuda() for s in range(n_shards)]
+
+
+def join_shards(shards, N):
+    return np.concatenate([s.cpu().numpy() for s in shards])[:N]
+
+
+def full_to_mats(full, layout, wl):
+    full = full.cpu().numpy() if hasattr(full, "cpu") else full
+    out = {}
+    for i, (r, c) in enumerate(wl.shapes):
+        if wl.is_matrix[i]:
+            off = layout.full_offsets[i]
+            out[i] = full[off: off + r * c].reshape(r, c).astype(np.float64)
+    return out
+
+
+def mats_to_full(mats, layout):
+    full = np.zeros(max(1, layout.full_numel), dtype=np.float32)
+    for i, X in mats.items():
+        off = layout.full_offsets[i]
+        full[off: off + X.size] = np.asarray(X, dtype=np.float32).reshape(-1)
+    return torch.from_numpy(full).cuda()
+
+
+def matrix_mask(wl, N):
+    mask = np.zeros(N, dtype=bool)
+    pos = 0
+    for i, (r, c) in enumerate(wl.shapes):
+        if wl.is_matrix[i]:
+            mask[pos:pos + r * c] = True
+        pos += r * c
+    return mask
+
+
+# ------------------------------------------------------------------ gather / scatter
+@pytest.mark.parametrize("n_shards", [1, 3, 8])
+def test_gather_scatter_bit_exact(capi, n_shards):
+    wl = inputs.WORKLOADS["ragged_small"]
+    lay = capi.muon_layout_create(wl.shapes, n_shards, 0, wl.is_matrix)
+    N = lay.numel
+    rng = np.random.default_rng(n_shards)
+    flat = rng.normal(size=N).astype(np.float32)
+    shards = split_shards(flat, n_shards)
+    full = torch.full((lay.full_numel,), float("nan"), device="cuda")
+    capi.muon_gather_full(lay, shards, full)
+    torch.cuda.synchronize()
+    o = ref.flat_layout(wl.shapes, n_shards, wl.is_matrix)
+    want = ref.gather_full(ref.shard_flat(flat, o), o)
+    got = full_to_mats(full, lay, wl)
+    for i in want:
+        assert np.array_equal(got[i].astype(np.float32), want[i].astype(np.float32)), i
+    # scatter of fresh values into sentinel shards touches matrix positions only
+    y = {i: rng.normal(size=want[i].shape).astype(np.float32) for i in want}
+    sent = split_shards(np.full(N, 7.0, dtype=np.float32), n_shards)
+    for s in sent:
+        s.fill_(7.0)
+    capi.muon_scatter_updates(lay, mats_to_full(y, lay), sent)
+    torch.cuda.synchronize()
+    back = np.concatenate([s.cpu().numpy() for s in sent])
+    want_sh = ref.scatter_updates(y, o, [np.full(o["L"], 7.0) for _ in range(n_shards)])
+    assert np.array_equal(back, np.concatenate(want_sh).astype(np.float32))
+
+
+# ------------------------------------------------------------------ Newton-Schulz on given inputs
+def spectrum_inputs(wl, seed):
+    rng = np.random.default_rng(seed)
+    mats = {}
+    for i, (r, c) in enumerate(wl.shapes):
+        if not wl.is_matrix[i]:
+            continue
+        k = min(r, c)
+        U, _ = np.linalg.qr(rng.normal(size=(r, k)))
+        V, _ = np.linalg.qr(rng.normal(size=(c, k)))
+        s = np.exp(rng.uniform(np.log(1e-3), 0.0, size=k))  # three decades of spectrum
+        mats[i] = (U * s) @ V.T * rng.uniform(1e-3, 10.0)
+    return mats
+
+
+@pytest.mark.parametrize("ns_dtype", [0, 1])
+@pytest.mark.parametrize("ns_steps", [5, 1, 0])
+def test_orthogonalize_full_vs_oracle(capi, ns_dtype, ns_steps):
+    wl = inputs.WORKLOADS["ragged_small"]
+    lay = capi.muon_layout_create(wl.shapes, 1, ns_dtype, wl.is_matrix)
+    ws = capi.workspace_tensor(lay)
+    X = spectrum_inputs(wl, 10 + ns_steps)
+    out = torch.zeros(lay.full_numel, device="cuda")
+    capi.muon_orthogonalize_full(lay, ws, mats_to_full(X, lay), out, ns_steps)
+    capi.muon_check()
+    got = full_to_mats(out, lay, wl)
+    for i, Xi in X.items():
+        want = ref.newton_schulz(Xi.astype(np.float32).astype(np.float64), ns_steps)
+        assert got[i].shape == want.shape
+        e = rel(got[i], want)
+        assert e < TOL_NS[ns_dtype], (i, wl.shapes[i], e)
+
+
+@pytest.mark.parametrize("ns_dtype", [0, 1])
+def test_orthogonalize_zero_matrix_gives_zero(capi, ns_dtype):
+    shapes = [(130, 300), (5, 5)]
+    lay = capi.muon_layout_create(shapes, 1, ns_dtype)
+    ws = capi.workspace_tensor(lay)
+    fin = torch.zeros(lay.full_numel, device="cuda")
+    off = lay.full_offsets[1]
+    fin[off: off + 25] = torch.arange(25, dtype=torch.float32, device="cuda") - 12
+    out = torch.full((lay.full_numel,), float("nan"), device="cuda")
+    capi.muon_orthogonalize_full(lay, ws, fin, out, 5)
+    capi.muon_check()
+    o = out.cpu().numpy()
+    assert np.all(o[:130 * 300] == 0.0)
+    want = ref.newton_schulz((np.arange(25.0) - 12).reshape(5, 5))
+    assert rel(o[off:off + 25].reshape(5, 5), want) < TOL_NS[ns_dtype]
+
+
+# ------------------------------------------------------------------ the step, stage by stage
+def run_steps(capi, wl, n_shards, ns_dtype, n_steps, check):
+    lay = capi.muon_layout_create(wl.shapes, n_shards, ns_dtype, wl.is_matrix)
+    ws = capi.workspace_tensor(lay)
+    N = lay.numel
+    W0, Gs, M0 = inputs.host_inputs(wl)
+    W = split_shards(W0, n_shards)
+    M = split_shards(M0, n_shards)
+    mask = matrix_mask(wl, N)
+    o = ref.flat_layout(wl.shapes, n_shards, wl.is_matrix)
+    fin = torch.zeros(max(1, lay.full_numel), device="cuda")
+    fout = torch.zeros(max(1, lay.full_numel), device="cuda")
+    M_or = M0.astype(np.float64)
+    for t in range(n_steps):
+        G = split_shards(Gs[t], n_shards)
+        W_prev = join_shards(W, N)
+        M_prev = join_shards(M, N)
+        capi.muon_compute_momentum_inputs(G, M, lay, ws, wl.mu, wl.nesterov)
+        capi.muon_export_input(lay, ws, fin)
+        capi.muon_orthogonalize_updates(lay, ws, wl.ns_steps)
+        capi.muon_export_update(lay, ws, wl.ns_steps, fout)
+        capi.muon_apply_local_updates(W, lay, ws, wl.lr, wl.wd, wl.ns_steps)
+        capi.muon_check()
+        W_new = join_shards(W, N)
+        M_new = join_shards(M, N)
+        # momentum, against the oracle's own running momentum (M never depends on W or O)
+        M_or = np.where(mask, ref.momentum_update(M_or, Gs[t], wl.mu), M_or)
+        assert rel(M_new[mask], M_or[mask]) < TOL_STATE
+        assert np.array_equal(M_new[~mask], M_prev[~mask])
+        X_gpu = full_to_mats(fin, lay, wl)
+        O_gpu = full_to_mats(fout, lay, wl)
+        X_or = ref.gather_full(ref.shard_flat(ref.ns_input(Gs[t], M_or, wl.mu, wl.nesterov), o), o)
+        for i in X_or:
+            r, c = wl.shapes[i]
+            assert rel(X_gpu[i], X_or[i]) < TOL_X[ns_dtype], ("X", i)
+            assert rel(O_gpu[i], ref.newton_schulz(X_gpu[i], wl.ns_steps)) < TOL_NS[ns_dtype], ("O", i)
+            assert rel(O_gpu[i], ref.newton_schulz(X_or[i], wl.ns_steps)) < TOL_NS[ns_dtype], ("O*", i)
+            off = o["offsets"][i]
+            Wp = W_prev[off: off + r * c].astype(np.float64)
+            want = ref.apply_update(ref.weight_decay(Wp, wl.lr, wl.wd), O_gpu[i].reshape(-1), wl.lr,
+                                    r, c)
+            assert rel(W_new[off: off + r * c], want) < TOL_STATE, ("W", i)
+        assert np.array_equal(W_new[~mask], W_prev[~mask])
+        # shard padding never touched
+        pad = np.concatenate([s.cpu().numpy() for s in W])[N:]
+        assert not pad.any()
+        if check is not None:
+            check(t, W, M)
+    return lay, W, M
+
+
+@pytest.mark.parametrize("ns_dtype", [0, 1])
+def test_single_256x128_three_steps(capi, ns_dtype):
+    run_steps(capi, inputs.WORKLOADS["single_256x128"], 1, ns_dtype, 3, None)
+
+
+@pytest.mark.parametrize("ns_dtype", [0, 1])
+@pytest.mark.parametrize("n_shards", [1, 3])
+def test_ragged_two_steps(capi, ns_dtype, n_shards):
+    run_steps(capi, inputs.WORKLOADS["ragged_small"], n_shards, ns_dtype, 2, None)
+
+
+@pytest.mark.parametrize("ns_dtype", [0, 1])
+def test_step_equals_stages_and_sharding_is_exact(capi, ns_dtype):
+    """muon_step = the three stage calls, bit for bit; 1 shard vs 5 shards bit for bit."""
+    wl = inputs.WORKLOADS["ragged_small"]
+    W0, Gs, M0 = inputs.host_inputs(wl)
+    results = []
+    for n_shards, fused in [(1, True), (5, True), (5, False)]:
+        lay = capi.muon_layout_create(wl.shapes, n_shards, ns_dtype, wl.is_matrix)
+        ws = capi.workspace_tensor(lay)
+        W = split_shards(W0, n_shards)
+        M = split_shards(M0, n_shards)
+        for t in range(2):
+            G = split_shards(Gs[t], n_shards)
+            if fused:
+                capi.muon_step(W, G, M, lay, ws, wl.lr, wl.wd, wl.mu, True, 5)
+            else:
+                capi.muon_compute_momentum_inputs(G, M, lay, ws, wl.mu, True)
+                capi.muon_orthogonalize_updates(lay, ws, 5)
+                capi.muon_apply_local_updates(W, lay, ws, wl.lr, wl.wd, 5)
+        capi.muon_check()
+        results.append((join_shards(W, lay.numel), join_shards(M, lay.numel)))
+    for Wr, Mr in results[1:]:
+        assert np.array_equal(Wr, results[0][0])
+        assert np.array_equal(Mr, results[0][1])
+
+
+def test_repeat_runs_are_bit_identical(capi):
+    wl = inputs.WORKLOADS["ragged_small"]
+    W0, Gs, M0 = inputs.host_inputs(wl)
+    outs = []
+    for _ in range(2):
+        lay = capi.muon_layout_create(wl.shapes, 2, 0, wl.is_matrix)
+        ws = capi.workspace_tensor(lay)
+        W, M, G = split_shards(W0, 2), split_shards(M0, 2), split_shards(Gs[0], 2)
+        capi.muon_step(W, G, M, lay, ws, wl.lr, wl.wd, wl.mu, True, 5)
+        capi.muon_check()
+        outs.append(join_shards(W, lay.numel))
+    assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("nesterov", [True, False])
+def test_plain_momentum_and_zero_ns_steps(capi, nesterov):
+    wl = inputs.WORKLOADS["single_256x128"]
+    W0, Gs, M0 = inputs.host_inputs(wl)
+    lay = capi.muon_layout_create(wl.shapes, 1, 1)
+    ws = capi.workspace_tensor(lay)
+    W, M, G = split_shards(W0, 1), split_shards(M0 + 0.5, 1), split_shards(Gs[0], 1)
+    capi.muon_step(W, G, M, lay, ws, wl.lr, wl.wd, wl.mu, nesterov, 0)
+    capi.muon_check()
+    Mo = ref.momentum_update(M0 + 0.5, Gs[0], wl.mu)
+    X = ref.ns_input(Gs[0], Mo, wl.mu, nesterov).reshape(256, 128)
+    O = ref.newton_schulz(X, 0)  # X / ||X||
+    want = ref.apply_update(ref.weight_decay(W0, wl.lr, wl.wd), O.reshape(-1), wl.lr, 256, 128)
+    assert rel(join_shards(M, lay.numel), Mo) < TOL_STATE
+    assert rel(join_shards(W, lay.numel), want) < 2e-6
+
+
+def test_empty_layout_is_a_noop(capi):
+    lay = capi.muon_layout_create([(4, 1)], 1, 0, [False])
+    ws = capi.workspace_tensor(lay)
+    W = torch.arange(4, dtype=torch.float32, device="cuda")
+    M = torch.ones(4, device="cuda")
+    G = torch.ones(4, device="cuda")
+    capi.muon_step([W], [G], [M], lay, ws, 0.02, 0.01, 0.95, True, 5)
+    capi.muon_check()
+    assert torch.equal(W.cpu(), torch.arange(4, dtype=torch.float32))
+    assert torch.equal(M.cpu(), torch.ones(4))
+
+
+def test_wait_timeout_is_reported_and_context_survives(capi):
+    capi.muon_check()  # clean slate
+    capi.muon_selftest_wait_timeout(1_000_000)
+    assert capi.muon_check_status() == capi.MUON_ERR_TIMEOUT
+    assert capi.muon_check_status() == capi.MUON_OK  # cleared
+    x = torch.ones(8, device="cuda") * 2
+    assert float(x.sum()) == 16.0
