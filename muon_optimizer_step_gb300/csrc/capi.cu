@@ -7,6 +7,7 @@
 // index maps fused into the first and last kernels.
 #include <cmath>
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -123,9 +124,20 @@ muon_status ensure_device(muon_layout* L) {
   if ((s = upload(L->plan.chunks, &t.chunks)) != MUON_OK) { free_tables(&t); return s; }
   if ((s = upload(L->plan.mats, &t.mats)) != MUON_OK) { free_tables(&t); return s; }
   const bool bf16 = L->plan.ns_dtype == MUON_NS_BF16;
+  int pairs = sms / 2;
+  if (bf16) {
+    const char* v = std::getenv("MUON_TC_KERNEL");
+    t.tc_variant = (v != nullptr && v[0] == '2') ? 2 : 1;
+    if (t.tc_variant == 2) {
+      e = prepare_tc2_kernel(&pairs);
+      if (e != cudaSuccess) { free_tables(&t); return cuda_fail(e, "prepare pair kernel"); }
+      if (pairs < 1) { free_tables(&t); return fail(MUON_ERR_UNSUPPORTED, "no CTA pair fits on the device"); }
+    }
+  }
   for (int p = 0; p < 3; ++p) {
-    const TileList tl = bf16 ? plan_tiles(L->plan, p, kTcBM, kTcBN, kTcBK, sms)
-                             : plan_tiles(L->plan, p, kF32BM, kF32BN, 16, sms);
+    const TileList tl = !bf16 ? plan_tiles(L->plan, p, kF32BM, kF32BN, 16, sms)
+                      : t.tc_variant == 2 ? plan_tiles(L->plan, p, 256, 256, kTcBK, pairs)
+                                          : plan_tiles(L->plan, p, kTcBM, kTcBN, kTcBK, sms);
     t.grid[p] = tl.grid;
     if ((s = upload(tl.tiles, &t.tiles[p])) != MUON_OK) { free_tables(&t); return s; }
     if ((s = upload(tl.cta_begin, &t.cta_begin[p])) != MUON_OK) { free_tables(&t); return s; }
@@ -219,10 +231,13 @@ muon_status run_ns(muon_layout* L, void* ws, int ns_steps, cudaStream_t st) {
     const int x_in = it & 1;
     const int iter0 = it == 0 ? 1 : 0;
     for (int ph = 0; ph < 3; ++ph) {
-      const cudaError_t e = L->plan.ns_dtype == MUON_NS_BF16
-                                ? launch_ns_phase_tc(L->plan, L->dt, ws, ph, x_in, iter0,
-                                                     kDefaultBudget, st)
-                                : launch_ns_phase_f32(L->plan, L->dt, ws, ph, x_in, iter0, st);
+      cudaError_t e;
+      if (L->plan.ns_dtype != MUON_NS_BF16)
+        e = launch_ns_phase_f32(L->plan, L->dt, ws, ph, x_in, iter0, st);
+      else if (L->dt.tc_variant == 2)
+        e = launch_ns_phase_tc2(L->plan, L->dt, ws, ph, x_in, iter0, kDefaultBudget, st);
+      else
+        e = launch_ns_phase_tc(L->plan, L->dt, ws, ph, x_in, iter0, kDefaultBudget, st);
       if (e != cudaSuccess) return cuda_fail(e, "newton_schulz phase");
     }
   }

@@ -21,6 +21,7 @@ struct DevTables {
   int32_t* cta_begin[3] = {nullptr, nullptr, nullptr};
   int grid[3] = {0, 0, 0};
   CUtensorMap* tmaps = nullptr; // kMapsPerMat per matrix (bf16 path)
+  int tc_variant = 1;           // bf16 path: 1 = single-CTA 128x256 tiles, 2 = CTA pairs 256x256
   const void* tmap_ws = nullptr;  // workspace the tensor maps were encoded for
 };
 
@@ -50,6 +51,11 @@ cudaError_t launch_export(const Plan& plan, const DevTables& dt, const void* ws,
 // Stage 2, bf16 path: one tcgen05 GEMM phase over every matrix.
 cudaError_t launch_ns_phase_tc(const Plan& plan, const DevTables& dt, void* ws, int phase,
                                int x_in, int iter0, long long budget, cudaStream_t st);
+// Stage 2, bf16 path on CTA pairs (tcgen05 cta_group::2): grid[phase] counts pairs.
+cudaError_t launch_ns_phase_tc2(const Plan& plan, const DevTables& dt, void* ws, int phase,
+                                int x_in, int iter0, long long budget, cudaStream_t st);
+// Shared-memory opt-in of the pair kernel and how many pairs can be resident at once.
+cudaError_t prepare_tc2_kernel(int* max_pairs);
 // Stage 2, fp32 path: one SIMT GEMM phase over every matrix.
 cudaError_t launch_ns_phase_f32(const Plan& plan, const DevTables& dt, void* ws, int phase,
                                 int x_in, int iter0, cudaStream_t st);

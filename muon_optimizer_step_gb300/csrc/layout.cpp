@@ -94,20 +94,25 @@ std::string build_plan(const int64_t* shapes, const uint8_t* is_matrix, int32_t 
     m.chunk_begin = (int64_t)p.chunks.size();
     const int64_t numel = (int64_t)m.rows * m.cols;
     const bool dense_x = (m.ldx == m.cols);
+    // Chunks are cut at fixed multiples of kChunkElems of the matrix's own row-major
+    // index, never at shard edges: the per-chunk sums of squares (and so ||X||) are then
+    // the same bits for every sharding of the same buffer.  A chunk that crosses a shard
+    // edge takes the kernels' per-element path.
     int64_t local = 0;
     while (local < numel) {
       const int64_t g = p.flat_off[i] + local;
       const int64_t s = g / p.L;
       const int64_t so = g - s * p.L;
-      int64_t len = std::min<int64_t>(kChunkElems, numel - local);
-      len = std::min<int64_t>(len, p.L - so);
+      const int64_t len = std::min<int64_t>(kChunkElems, numel - local);
       ChunkDev ch{};
       ch.mat = (int32_t)p.mats.size();
       ch.shard = (int32_t)s;
       ch.shard_off = so;
       ch.local = local;
       ch.len = (int32_t)len;
-      ch.vec = (so % 4 == 0 && local % 4 == 0 && m.full_off % 4 == 0 && dense_x) ? 1 : 0;
+      const bool one_shard = so + len <= p.L;
+      ch.vec = (one_shard && so % 4 == 0 && local % 4 == 0 && m.full_off % 4 == 0 && dense_x)
+                   ? 1 : 0;
       p.chunks.push_back(ch);
       local += len;
     }

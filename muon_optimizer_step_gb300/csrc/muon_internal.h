@@ -10,7 +10,9 @@
 namespace muon {
 
 // Flat elements handled by one entry of the chunk table.  A chunk never crosses a
-// matrix boundary or a shard edge, so a kernel reads it through one shard pointer.
+// matrix boundary; it starts at a multiple of kChunkElems of the matrix's row-major
+// index.  One that lies inside one shard (the usual case) is read through that shard's
+// pointer with 128-bit loads; one that crosses a shard edge is read element by element.
 constexpr int kChunkElems = 32768;
 
 // Workspace alignment of every per-matrix buffer (TMA wants 16 B; SW128 tiles 1024 B).
@@ -36,11 +38,11 @@ enum Phase { kPhaseGram = 0, kPhasePoly = 1, kPhaseUpdate = 2 };
 
 struct ChunkDev {          // 32 bytes
   int32_t mat;             // matrix index (dense, over matrix parameters only)
-  int32_t shard;           // shard holding the whole chunk
-  int64_t shard_off;       // element offset inside that shard
+  int32_t shard;           // shard holding the chunk's first element
+  int64_t shard_off;       // its offset inside that shard
   int64_t local;           // row-major element index inside the matrix
   int32_t len;             // elements in the chunk
-  int32_t vec;             // 1: shard_off, local, full offset and length allow float4
+  int32_t vec;             // 1: inside one shard, and offsets allow 128-bit accesses
 };
 
 struct MatDev {            // 96 bytes

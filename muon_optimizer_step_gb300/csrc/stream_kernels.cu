@@ -9,8 +9,10 @@
 //    place (the owner scatter, as indexing), W written in shard order.
 //  * gather / scatter / export / full_input: the same index map as bit copies.
 //
-// Every kernel walks the chunk table: a chunk lies inside one matrix and one shard, so a
-// block reads it through one shard pointer with 128-bit loads when offsets allow.
+// Every kernel walks the chunk table: a chunk lies inside one matrix, at a fixed place of
+// its row-major index.  Inside one shard a block reads it with 128-bit accesses; across a
+// shard edge it reads it element by element, in the same per-thread order, so that the
+// per-chunk sums of squares do not depend on how the buffer is sharded.
 #include "device_common.cuh"
 #include "kernels.h"
 
@@ -60,6 +62,27 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return s;
 }
 
+// Sum-of-squares updates with explicit rounding (no FMA contraction), so that the
+// 128-bit path and the per-element path add the same terms in the same order.
+__device__ __forceinline__ float add_sq4(float ss, float a, float b, float c, float d) {
+  return __fadd_rn(ss, __fadd_rn(__fadd_rn(__fmul_rn(a, a), __fmul_rn(b, b)),
+                                 __fadd_rn(__fmul_rn(c, c), __fmul_rn(d, d))));
+}
+__device__ __forceinline__ float add_sq1(float ss, float a) { return __fadd_rn(ss, __fmul_rn(a, a)); }
+
+// Element t of a chunk in the shards (a chunk may cross shard edges).
+__device__ __forceinline__ float* elem_ptr(const ShardPtrs& P, const ChunkDev& ch, int64_t L,
+                                           int64_t t) {
+  int64_t o = ch.shard_off + t;
+  int s = ch.shard;
+  if (o >= L) {
+    const int64_t q = o / L;
+    s += (int)q;
+    o -= q * L;
+  }
+  return P.p[s] + o;
+}
+
 // Position of row-major element `local` of a matrix in its pitched X buffer.
 __device__ __forceinline__ int64_t x_index(const MatDev& mt, int64_t local) {
   if (mt.ldx == mt.cols) return local;
@@ -70,22 +93,22 @@ __device__ __forceinline__ int64_t x_index(const MatDev& mt, int64_t local) {
 template <typename XT>
 __global__ void __launch_bounds__(kThreads)
 momentum_input_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
-                      const MatDev* __restrict__ mats, ShardPtrs G, ShardPtrs M,
+                      const MatDev* __restrict__ mats, ShardPtrs G, ShardPtrs M, int64_t L,
                       uint8_t* __restrict__ ws, float* __restrict__ partials, float mu,
                       int nesterov) {
   __shared__ float red[32];
   for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
     const ChunkDev ch = chunks[ci];
     const MatDev& mt = mats[ch.mat];
-    const float* __restrict__ g = G.p[ch.shard] + ch.shard_off;
-    float* __restrict__ m = M.p[ch.shard] + ch.shard_off;
     XT* __restrict__ x = reinterpret_cast<XT*>(ws + mt.x0);
+    const int nv = ch.len >> 2;
     float ss = 0.f;
     if (ch.vec) {
+      const float* g = G.p[ch.shard] + ch.shard_off;
+      float* m = M.p[ch.shard] + ch.shard_off;
       XT* xv = x + ch.local;
       const float4* g4 = reinterpret_cast<const float4*>(g);
       float4* m4 = reinterpret_cast<float4*>(m);
-      const int nv = ch.len >> 2;
       int v = threadIdx.x;
       for (; v + 3 * kThreads < nv; v += 4 * kThreads) {
         float4 gv[4], mv[4];
@@ -111,7 +134,7 @@ momentum_input_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
           }
           __stcs(m4 + v + u * kThreads, mn);
           store4(xv + 4 * (v + u * kThreads), xn.x, xn.y, xn.z, xn.w);
-          ss += xn.x * xn.x + xn.y * xn.y + xn.z * xn.z + xn.w * xn.w;
+          ss = add_sq4(ss, xn.x, xn.y, xn.z, xn.w);
         }
       }
       for (; v < nv; v += kThreads) {
@@ -132,22 +155,40 @@ momentum_input_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
         }
         __stcs(m4 + v, mn);
         store4(xv + 4 * v, xn.x, xn.y, xn.z, xn.w);
-        ss += xn.x * xn.x + xn.y * xn.y + xn.z * xn.z + xn.w * xn.w;
+        ss = add_sq4(ss, xn.x, xn.y, xn.z, xn.w);
       }
       for (int t = nv * 4 + threadIdx.x; t < ch.len; t += kThreads) {
         const float mn = fmaf(mu, m[t], g[t]);
         const float xn = nesterov ? fmaf(mu, mn, g[t]) : mn;
         m[t] = mn;
         store1(xv + t, xn);
-        ss += xn * xn;
+        ss = add_sq1(ss, xn);
       }
     } else {
-      for (int t = threadIdx.x; t < ch.len; t += kThreads) {
-        const float mn = fmaf(mu, m[t], g[t]);
-        const float xn = nesterov ? fmaf(mu, mn, g[t]) : mn;
-        m[t] = mn;
+      // Same element-to-thread assignment and summation order as the 128-bit path.
+      for (int v = threadIdx.x; v < nv; v += kThreads) {
+        float xs[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = 4 * v + e;
+          const float gt = *elem_ptr(G, ch, L, t);
+          float* mp = elem_ptr(M, ch, L, t);
+          const float mn = fmaf(mu, *mp, gt);
+          const float xn = nesterov ? fmaf(mu, mn, gt) : mn;
+          *mp = mn;
+          store1(x + x_index(mt, ch.local + t), xn);
+          xs[e] = xn;
+        }
+        ss = add_sq4(ss, xs[0], xs[1], xs[2], xs[3]);
+      }
+      for (int t = nv * 4 + threadIdx.x; t < ch.len; t += kThreads) {
+        const float gt = *elem_ptr(G, ch, L, t);
+        float* mp = elem_ptr(M, ch, L, t);
+        const float mn = fmaf(mu, *mp, gt);
+        const float xn = nesterov ? fmaf(mu, mn, gt) : mn;
+        *mp = mn;
         store1(x + x_index(mt, ch.local + t), xn);
-        ss += xn * xn;
+        ss = add_sq1(ss, xn);
       }
     }
     const float tot = block_sum(ss, red);
@@ -170,7 +211,7 @@ full_input_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
     for (int t = threadIdx.x; t < ch.len; t += kThreads) {
       const float v = src[t];
       store1(x + x_index(mt, ch.local + t), v);
-      ss += v * v;
+      ss = add_sq1(ss, v);
     }
     const float tot = block_sum(ss, red);
     if (threadIdx.x == 0) partials[ci] = tot;
@@ -200,7 +241,8 @@ norm_finalize_kernel(const MatDev* __restrict__ mats, int n_mats,
 template <typename XT>
 __global__ void __launch_bounds__(kThreads)
 apply_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
-             const MatDev* __restrict__ mats, ShardPtrs W, const uint8_t* __restrict__ ws,
+             const MatDev* __restrict__ mats, ShardPtrs W, int64_t L,
+             const uint8_t* __restrict__ ws,
              int final_buf, const float* __restrict__ inv_norm, int pending_norm, float decay,
              float lr) {
   for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
@@ -209,8 +251,8 @@ apply_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
     float lrs = lr * mt.scale;
     if (pending_norm) lrs *= inv_norm[ch.mat];
     const XT* __restrict__ o = reinterpret_cast<const XT*>(ws + (final_buf ? mt.x1 : mt.x0));
-    float* __restrict__ w = W.p[ch.shard] + ch.shard_off;
     if (ch.vec) {
+      float* __restrict__ w = W.p[ch.shard] + ch.shard_off;
       const XT* ov = o + ch.local;
       float4* w4 = reinterpret_cast<float4*>(w);
       const int nv = ch.len >> 2;
@@ -245,44 +287,47 @@ apply_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
       for (int t = nv * 4 + threadIdx.x; t < ch.len; t += kThreads)
         w[t] = fmaf(-lrs, load1(ov + t), w[t] * decay);
     } else {
-      for (int t = threadIdx.x; t < ch.len; t += kThreads)
-        w[t] = fmaf(-lrs, load1(o + x_index(mt, ch.local + t)), w[t] * decay);
+      for (int t = threadIdx.x; t < ch.len; t += kThreads) {
+        float* wp = elem_ptr(W, ch, L, t);
+        *wp = fmaf(-lrs, load1(o + x_index(mt, ch.local + t)), *wp * decay);
+      }
     }
   }
 }
 
 __global__ void __launch_bounds__(kThreads)
 gather_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
-              const MatDev* __restrict__ mats, ShardPtrs S, float* __restrict__ full) {
+              const MatDev* __restrict__ mats, ShardPtrs S, int64_t L, float* __restrict__ full) {
   for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
     const ChunkDev ch = chunks[ci];
-    const float* src = S.p[ch.shard] + ch.shard_off;
     float* dst = full + mats[ch.mat].full_off + ch.local;
     if (ch.vec) {
+      const float* src = S.p[ch.shard] + ch.shard_off;
       const int nv = ch.len >> 2;
       for (int v = threadIdx.x; v < nv; v += kThreads)
         reinterpret_cast<float4*>(dst)[v] = reinterpret_cast<const float4*>(src)[v];
       for (int t = nv * 4 + threadIdx.x; t < ch.len; t += kThreads) dst[t] = src[t];
     } else {
-      for (int t = threadIdx.x; t < ch.len; t += kThreads) dst[t] = src[t];
+      for (int t = threadIdx.x; t < ch.len; t += kThreads) dst[t] = *elem_ptr(S, ch, L, t);
     }
   }
 }
 
 __global__ void __launch_bounds__(kThreads)
 scatter_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
-               const MatDev* __restrict__ mats, const float* __restrict__ full, ShardPtrs D) {
+               const MatDev* __restrict__ mats, const float* __restrict__ full, ShardPtrs D,
+               int64_t L) {
   for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
     const ChunkDev ch = chunks[ci];
-    float* dst = D.p[ch.shard] + ch.shard_off;
     const float* src = full + mats[ch.mat].full_off + ch.local;
     if (ch.vec) {
+      float* dst = D.p[ch.shard] + ch.shard_off;
       const int nv = ch.len >> 2;
       for (int v = threadIdx.x; v < nv; v += kThreads)
         reinterpret_cast<float4*>(dst)[v] = reinterpret_cast<const float4*>(src)[v];
       for (int t = nv * 4 + threadIdx.x; t < ch.len; t += kThreads) dst[t] = src[t];
     } else {
-      for (int t = threadIdx.x; t < ch.len; t += kThreads) dst[t] = src[t];
+      for (int t = threadIdx.x; t < ch.len; t += kThreads) *elem_ptr(D, ch, L, t) = src[t];
     }
   }
 }
@@ -320,10 +365,10 @@ cudaError_t launch_momentum_input(const Plan& plan, const DevTables& dt, const S
   float* partials = reinterpret_cast<float*>(w + plan.ws_partials);
   if (plan.ns_dtype == 0)
     momentum_input_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
-        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, w, partials, mu, nesterov);
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, plan.L, w, partials, mu, nesterov);
   else
     momentum_input_kernel<float><<<grid, kThreads, 0, st>>>(
-        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, w, partials, mu, nesterov);
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, plan.L, w, partials, mu, nesterov);
   return cudaGetLastError();
 }
 
@@ -363,11 +408,11 @@ cudaError_t launch_apply(const Plan& plan, const DevTables& dt, const ShardPtrs&
   const float* inv = reinterpret_cast<const float*>(w + plan.ws_inv_norm);
   if (plan.ns_dtype == 0)
     apply_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
-        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, wp, w, final_buf, inv, pending_norm,
-        decay, lr);
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, wp, plan.L, w, final_buf, inv,
+        pending_norm, decay, lr);
   else
     apply_kernel<float><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
-                                                   dt.mats, wp, w, final_buf, inv,
+                                                   dt.mats, wp, plan.L, w, final_buf, inv,
                                                    pending_norm, decay, lr);
   return cudaGetLastError();
 }
@@ -377,7 +422,7 @@ cudaError_t launch_gather(const Plan& plan, const DevTables& dt, const ShardPtrs
   const int grid = grid_for(plan, dt);
   if (grid == 0) return cudaSuccess;
   gather_kernel<<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(), dt.mats,
-                                           src, full);
+                                           src, plan.L, full);
   return cudaGetLastError();
 }
 
@@ -386,7 +431,7 @@ cudaError_t launch_scatter(const Plan& plan, const DevTables& dt, const float* f
   const int grid = grid_for(plan, dt);
   if (grid == 0) return cudaSuccess;
   scatter_kernel<<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(), dt.mats,
-                                            full, dst);
+                                            full, dst, plan.L);
   return cudaGetLastError();
 }
 
