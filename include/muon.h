@@ -156,6 +156,31 @@ muon_status muon_export_input(const muon_layout* layout, const void* workspace,
 muon_status muon_export_update(const muon_layout* layout, const void* workspace,
                                int32_t ns_steps, float* full_out, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- allocation-free variant
+ * muon_orthogonalize_full_noalloc: muon_orthogonalize_full without any device allocation.
+ * The paper has no counterpart to this entry point.  It is for callers that cannot call
+ * cudaMalloc, nor have the library call it, where the orthogonalization runs: a host
+ * framework whose caching allocator owns the device memory pool, a latency-critical loop
+ * that cannot afford the synchronisation cudaMalloc / cudaFree may imply, a plugin inside
+ * a process where only the host application allocates device memory.
+ *   layout    a layout created with ns_dtype = MUON_NS_FP32 (the fp32 CUDA-core path);
+ *             bf16 layouts return MUON_ERR_UNSUPPORTED.
+ *   full_in   device, fp32 full layout (muon_full_offsets), 16-byte aligned: the inputs.
+ *   full_out  device, same layout, 16-byte aligned: receives the orthogonalized updates.
+ * Everything else (the layout's device tables and the workspace) lives in one file-scope
+ * device array of 32 MiB (33,554,432 bytes) that every GPU loading the library holds until
+ * the process exits.  A layout whose tables plus workspace exceed it is rejected with
+ * MUON_ERR_UNSUPPORTED and a message giving both sizes.  The call allocates no device
+ * memory (no cudaMalloc, cudaFree or allocating library routine); it uses host memory for
+ * planning and cudaMemcpyAsync into the array.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls share the array and leave their data in it:
+ * calls that overlap on the GPU (different streams or threads) race.  Results equal those
+ * of muon_orthogonalize_full on an fp32 layout. */
+muon_status muon_orthogonalize_full_noalloc(const muon_layout* layout, const float* full_in,
+                                            float* full_out, int32_t ns_steps,
+                                            cudaStream_t stream);
+
 /* ---------------------------------------------------------------- status
  * Synchronises `stream`, then reports a device-side wait timeout recorded since the last
  * check (MUON_ERR_TIMEOUT, and clears it) or a CUDA error (MUON_ERR_CUDA). */

@@ -55,6 +55,7 @@ SIGNATURES = [
     ("muon_orthogonalize_full", _I32, [_P, _P, _P, _P, _I32, _P]),
     ("muon_export_input", _I32, [_P, _P, _P, _P]),
     ("muon_export_update", _I32, [_P, _P, _I32, _P, _P]),
+    ("muon_orthogonalize_full_noalloc", _I32, [_P, _P, _P, _I32, _P]),
     ("muon_check", _I32, [_P]),
     ("muon_selftest_wait_timeout", _I32, [_I64, _P]),
 ]
@@ -238,6 +239,15 @@ def muon_orthogonalize_full(layout, workspace, full_in, full_out, ns_steps=5, st
     _check(lib.muon_orthogonalize_full(layout.handle, _ptr(workspace), _ptr(full_in),
                                        _ptr(full_out), int(ns_steps), _stream_handle(stream)),
            "muon_orthogonalize_full")
+
+
+def muon_orthogonalize_full_noalloc(layout, full_in, full_out, ns_steps=5, stream=None):
+    """Like muon_orthogonalize_full, but with no workspace argument and no device
+    allocation: for callers that cannot allocate device memory where they orthogonalize
+    (fp32 layouts up to 32 MiB of tables plus workspace; see include/muon.h)."""
+    _check(lib.muon_orthogonalize_full_noalloc(layout.handle, _ptr(full_in), _ptr(full_out),
+                                               int(ns_steps), _stream_handle(stream)),
+           "muon_orthogonalize_full_noalloc")
 
 
 def muon_export_input(layout, workspace, full_out, stream=None):

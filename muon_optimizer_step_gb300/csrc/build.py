@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libmuon.so")
 
 SOURCES = ["layout.cpp", "capi.cu", "stream_kernels.cu", "gemm_f32.cu", "gemm_tc.cu",
-           "gemm_tc2.cu"]
+           "gemm_tc2.cu", "noalloc.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

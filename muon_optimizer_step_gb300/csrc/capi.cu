@@ -20,11 +20,7 @@
 
 using namespace muon;
 
-struct muon_layout {
-  Plan plan;
-  DevTables dt;
-  std::mutex mu;
-};
+#include "layout_handle.h"
 
 namespace {
 
@@ -259,6 +255,8 @@ muon_status check_scalars(float lr, float wd, float mu) {
 }
 
 }  // namespace
+
+void muon::set_last_error(const std::string& msg) { g_last_error = msg; }
 
 extern "C" {
 

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <cuda.h>
 
+#include <string>
+
 #include "muon_internal.h"
 
 namespace muon {
@@ -64,6 +66,8 @@ bool encode_tensor_maps(const Plan& plan, const void* ws, std::vector<CUtensorMa
                         std::string* err);
 // One-block kernel that waits on an mbarrier nobody arrives on, with `budget` cycles.
 cudaError_t launch_selftest_timeout(int* err, long long budget, cudaStream_t st);
+// Sets the message muon_last_error() returns on this thread.
+void set_last_error(const std::string& msg);
 // Prepares the tcgen05 kernel (shared-memory opt-in) on the current device.
 cudaError_t prepare_tc_kernel();
 
