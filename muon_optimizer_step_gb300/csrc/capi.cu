@@ -121,19 +121,39 @@ muon_status ensure_device(muon_layout* L) {
   if ((s = upload(L->plan.mats, &t.mats)) != MUON_OK) { free_tables(&t); return s; }
   const bool bf16 = L->plan.ns_dtype == MUON_NS_BF16;
   int pairs = sms / 2;
+  int forced = 0;  // MUON_TC_KERNEL=1 or 2 pins one tcgen05 variant (for measurements)
   if (bf16) {
     const char* v = std::getenv("MUON_TC_KERNEL");
-    t.tc_variant = (v != nullptr && v[0] == '2') ? 2 : 1;
-    if (t.tc_variant == 2) {
-      e = prepare_tc2_kernel(&pairs);
-      if (e != cudaSuccess) { free_tables(&t); return cuda_fail(e, "prepare pair kernel"); }
-      if (pairs < 1) { free_tables(&t); return fail(MUON_ERR_UNSUPPORTED, "no CTA pair fits on the device"); }
-    }
+    if (v != nullptr && (v[0] == '1' || v[0] == '2')) forced = v[0] - '0';
+    e = prepare_tc2_kernel(&pairs);
+    if (e != cudaSuccess) { free_tables(&t); return cuda_fail(e, "prepare pair kernel"); }
+    if (pairs > sms / 2) pairs = sms / 2;
   }
   for (int p = 0; p < 3; ++p) {
-    const TileList tl = !bf16 ? plan_tiles(L->plan, p, kF32BM, kF32BN, 16, sms)
-                      : t.tc_variant == 2 ? plan_tiles(L->plan, p, 256, 256, kTcBK, pairs)
-                                          : plan_tiles(L->plan, p, kTcBM, kTcBN, kTcBK, sms);
+    TileList tl;
+    if (!bf16) {
+      tl = plan_tiles(L->plan, p, kF32BM, kF32BN, 16, sms);
+    } else {
+      // Per phase: CTA pairs (256 x 256 tiles, a third less operand traffic per k-block)
+      // when most of the phase's MMA work sits in matrices that span at least ten 256-wide
+      // tiles; single CTAs (128 x 256 tiles) otherwise, where the finer tiles balance
+      // better.  Measured on GB300: pairs are 4-7% faster on the Llama-3-8B set and 7-10%
+      // slower on the GPT-2 and MoE sets.
+      TileList t1 = plan_tiles(L->plan, p, kTcBM, kTcBN, kTcBK, sms);
+      double big = 0.0, all = 0.0;
+      for (const TileDev& td : t1.tiles) {
+        all += td.kblocks;
+        if (L->plan.mats[td.mat].m >= 2560) big += td.kblocks;
+      }
+      int variant = (pairs >= 1 && big >= 0.5 * all) ? 2 : 1;
+      if (forced != 0) variant = forced;
+      if (variant == 2 && pairs < 1) {
+        free_tables(&t);
+        return fail(MUON_ERR_UNSUPPORTED, "no CTA pair fits on the device");
+      }
+      t.tc_variant[p] = variant;
+      tl = variant == 2 ? plan_tiles(L->plan, p, 256, 256, kTcBK, pairs) : std::move(t1);
+    }
     t.grid[p] = tl.grid;
     if ((s = upload(tl.tiles, &t.tiles[p])) != MUON_OK) { free_tables(&t); return s; }
     if ((s = upload(tl.cta_begin, &t.cta_begin[p])) != MUON_OK) { free_tables(&t); return s; }
@@ -230,7 +250,7 @@ muon_status run_ns(muon_layout* L, void* ws, int ns_steps, cudaStream_t st) {
       cudaError_t e;
       if (L->plan.ns_dtype != MUON_NS_BF16)
         e = launch_ns_phase_f32(L->plan, L->dt, ws, ph, x_in, iter0, st);
-      else if (L->dt.tc_variant == 2)
+      else if (L->dt.tc_variant[ph] == 2)
         e = launch_ns_phase_tc2(L->plan, L->dt, ws, ph, x_in, iter0, kDefaultBudget, st);
       else
         e = launch_ns_phase_tc(L->plan, L->dt, ws, ph, x_in, iter0, kDefaultBudget, st);

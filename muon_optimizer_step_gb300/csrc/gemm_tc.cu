@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_phase_tc_kernel(const TcPar
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 128);
+      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
     }
     mbar_init(mma_done, 1);
     abort_flag = 0;
@@ -350,7 +350,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_phase_tc_kernel(const TcPar
         epilogue_chunk(p, mt, i, tile.j0 + 32 * c, v, s);
       }
       tc_fence_before();
-      mbar_arrive(&acc_empty[ab]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);
     }
   }
   tc_fence_before();

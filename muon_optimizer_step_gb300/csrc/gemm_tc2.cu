@@ -13,9 +13,10 @@
 // Per SM this halves the B-operand traffic of a 128 x 256 single-CTA tile (32 KB instead
 // of 48 KB per k-block for the same MMA work).
 //
-// Synchronisation: the even CTA's full[s] barrier counts both CTAs' arrivals and bytes;
-// the MMA commit multicasts to both CTAs' empty[s] and acc_full[b]; acc_empty[b] of the
-// even CTA counts the 256 epilogue threads of the pair.  Every wait is bounded.
+// Synchronisation: the even CTA's full[s] barrier takes one arrival (the even producer,
+// announcing both CTAs' bytes) and both CTAs' copies; the MMA commit multicasts to both
+// CTAs' empty[s] and acc_full[b]; acc_empty[b] of the even CTA counts one arrival per
+// epilogue warp of the pair (8).  Every wait is bounded.
 #include <cstdio>
 #include <string>
 #include <vector>
@@ -31,7 +32,7 @@ namespace {
 
 constexpr int BM = 256, BN = 256, BK = kTcBK;   // pair tile
 constexpr int HM = 128;                         // rows per CTA (of A and of B)
-constexpr int STAGES = 6;
+constexpr int STAGES = 7;
 constexpr int UMMA_K = 16;
 constexpr int A_BYTES = HM * BK * 2;            // 16 KB
 constexpr int B_BYTES = HM * BK * 2;            // 16 KB
@@ -208,12 +209,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 2);   // one arrival per CTA of the pair (+ both CTAs' bytes)
+      mbar_init(&full[s], 1);   // the even CTA's arrival, expecting both CTAs' bytes
       mbar_init(&empty[s], 1);  // the MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 2 * 128);
+      mbar_init(&acc_empty[b], 2 * 4);  // one arrival per epilogue warp of the pair
     }
     mbar_init(mma_done, 1);
     abort_flag = 0;
@@ -253,7 +254,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sb = sa + A_BYTES;
           const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
           const int k0 = kb * BK;
-          mbar_arrive_expect_tx_cluster(fbar, STAGE_BYTES);
+          // Only the even CTA arrives, announcing both CTAs' bytes; the odd CTA's copies may
+          // land first (the transaction count then dips below zero, which mbarriers allow,
+          // and the phase still needs the even CTA's arrival to complete).
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
           if (ops.a_mn) {
             tma_load_2d_pair(sa, amap, ia, k0, fbar);
             tma_load_2d_pair(sa + MN_BOX_BYTES, amap, ia + 64, k0, fbar);
@@ -359,7 +363,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         epilogue_chunk(p, mt, i, tile.j0 + 32 * c, v, s);
       }
       tc_fence_before();
-      mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[ab]), 0));
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(&acc_empty[ab]);
+        else mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[ab]), 0));
+      }
     }
   }
   tc_fence_before();

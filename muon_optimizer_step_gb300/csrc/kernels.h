@@ -23,7 +23,8 @@ struct DevTables {
   int32_t* cta_begin[3] = {nullptr, nullptr, nullptr};
   int grid[3] = {0, 0, 0};
   CUtensorMap* tmaps = nullptr; // kMapsPerMat per matrix (bf16 path)
-  int tc_variant = 1;           // bf16 path: 1 = single-CTA 128x256 tiles, 2 = CTA pairs 256x256
+  int tc_variant[3] = {2, 2, 2}; // bf16 path, per phase: 1 = single CTA 128x256 tiles,
+                                 // 2 = CTA pairs 256x256 tiles (grid[] then counts pairs)
   const void* tmap_ws = nullptr;  // workspace the tensor maps were encoded for
 };
 

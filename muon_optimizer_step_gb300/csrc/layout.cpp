@@ -196,4 +196,16 @@ TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_s
   return tl;
 }
 
+int64_t tile_makespan(const TileList& tl, int phase, int per_tile_units) {
+  int64_t worst = 0;
+  const int64_t epi = phase == kPhaseUpdate ? 2 : 3;
+  for (int c = 0; c < tl.grid; ++c) {
+    int64_t load = 0;
+    for (int t = tl.cta_begin[c]; t < tl.cta_begin[c + 1]; ++t)
+      load += (int64_t)per_tile_units * (tl.tiles[t].kblocks + epi);
+    worst = std::max(worst, load);
+  }
+  return worst;
+}
+
 }  // namespace muon

@@ -100,4 +100,8 @@ std::string build_plan(const int64_t* shapes, const uint8_t* is_matrix, int32_t 
 // Longest-processing-time assignment of a phase's tiles to `grid` CTAs (grid <= n_sms).
 TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_sms);
 
+// Largest per-CTA load of a tile list, in the cost units plan_tiles balances
+// (k-blocks of 128 x 256 x 64 MMA work plus an epilogue allowance per tile).
+int64_t tile_makespan(const TileList& tl, int phase, int per_tile_units);
+
 }  // namespace muon

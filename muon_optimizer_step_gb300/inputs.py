@@ -81,6 +81,9 @@ def _workloads():
     groups = tuple((3 * e, 3) for e in range(64))
     w["moe_64e"] = Workload("moe_64e", _mats(sh), (True,) * len(sh), 1, seed=3, rank=8,
                             expert_groups=groups)
+    sh = _LLAMA_LAYER * 2
+    w["llama3_8b_x2"] = Workload("llama3_8b_x2", _mats(sh), (True,) * len(sh), 1, seed=6,
+                                 rank=16)
     sh = ((4096, 1),) + _LLAMA_LAYER * 32
     w["llama3_8b_8shards"] = Workload("llama3_8b_8shards", _mats(sh),
                                       (False,) + (True,) * (len(sh) - 1), 8, seed=4, rank=16)

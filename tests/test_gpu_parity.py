@@ -318,3 +318,22 @@ def test_wait_timeout_is_reported_and_context_survives(capi):
     assert capi.muon_check_status() == capi.MUON_OK  # cleared
     x = torch.ones(8, device="cuda") * 2
     assert float(x.sum()) == 16.0
+
+
+@pytest.mark.parametrize("variant", ["1", "2"])
+def test_each_tcgen05_variant_vs_oracle(capi, variant, monkeypatch):
+    """Both tcgen05 kernels (single CTA 128x256 tiles, CTA pairs 256x256 tiles), pinned
+    one at a time, on ragged shapes and on a matrix that spans several pair tiles."""
+    monkeypatch.setenv("MUON_TC_KERNEL", variant)
+    shapes = [(300, 200), (130, 520), (7, 3), (64, 1000), (257, 129), (600, 1100)]
+    wl = inputs.Workload("mixed", tuple(shapes), (True,) * len(shapes), 1, seed=9, rank=4)
+    lay = capi.muon_layout_create(wl.shapes, 1, 0, wl.is_matrix)
+    ws = capi.workspace_tensor(lay)
+    X = recipe_inputs(wl, 3)
+    out = torch.zeros(lay.full_numel, device="cuda")
+    capi.muon_orthogonalize_full(lay, ws, mats_to_full(X, lay), out, 5)
+    capi.muon_check()
+    got = full_to_mats(out, lay, wl)
+    for i, Xi in X.items():
+        e = rel(got[i], ref.newton_schulz(Xi.astype(np.float32).astype(np.float64), 5))
+        assert e < TOL_NS[0], (variant, wl.shapes[i], e)
