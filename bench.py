@@ -58,6 +58,41 @@ def elementwise_bytes(n_matrix_elems, ns_dtype):
     return n_matrix_elems * (12 + x), n_matrix_elems * (8 + x)
 
 
+# DRAM bytes per Newton-Schulz launch (mean over Gram / Poly / Update) measured with ncu
+# on two Llama-3-8B layers and scaled by 16 to the 32-layer set (profiles/
+# ns_phase_tc2_llama3_8b_x2.md), valid only for the kernel sources it was taken with.
+NS_TRAFFIC = {
+    "llama3_8b_x32": {"bytes_per_launch": 16 * (1643911680 + 308051200 + 393551616 + 301336832
+                                                + 1937092352 + 840659712) / 3,
+                      "sources_sha256": "f6526958530d68364d2649d541e6b0ea1706db09ebc38f81b90bd1fcb22a7cdd"
+                                        "4a62cde6d76fdc1497b832035d8dcc9600b51a7c28220f28889df8a0430e42ae"
+                                        "2108b28e80686f6387a0970aac095580cb0cd4e61b4e7650c1da99dcdd7d86f0"},
+}
+
+
+def _ns_sources_sha256():
+    import hashlib
+    out = ""
+    for f in ("gemm_tc2.cu", "gemm_tc.cu", "layout.cpp"):
+        with open(os.path.join(ROOT, "muon_optimizer_step_gb300", "csrc", f), "rb") as fh:
+            out += hashlib.sha256(fh.read()).hexdigest()
+    return out
+
+
+def ns_traffic(workload, ns_dtype):
+    """Measured DRAM bytes per Newton-Schulz launch, or None if not measured for this
+    workload or if the kernel sources changed since the counters were taken."""
+    rec = NS_TRAFFIC.get(workload)
+    if rec is None or ns_dtype != "bf16":
+        return None
+    try:
+        if _ns_sources_sha256() != rec["sources_sha256"]:
+            return None
+    except OSError:
+        return None
+    return rec["bytes_per_launch"]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -221,6 +256,28 @@ def _mem_available_bytes():
     return 0
 
 
+def _pin_to_gpu_numa_node(dev):
+    """Run this thread on the CPUs next to the GPU, so pinned pages land on its node."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(dev)
+        bus = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        with open(f"/sys/bus/pci/devices/{bus}/local_cpulist") as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            if "-" in part:
+                lo, hi = part.split("-")
+                cpus.update(range(int(lo), int(hi) + 1))
+            elif part:
+                cpus.add(int(part))
+        cpus &= os.sched_getaffinity(0)
+        if cpus:
+            os.sched_setaffinity(0, cpus)
+    except (OSError, AttributeError, ValueError):
+        pass
+
+
 def run_ours(args):
     import torch
     from muon_optimizer_step_gb300 import capi, inputs
@@ -304,41 +361,74 @@ def run_ours(args):
     ms = total_ms / args.steps
 
     # ------------------------------------------------------------ end to end (host buffers)
+    # Every step takes its gradient from pinned host memory and returns its updated
+    # weights to pinned host memory, through the public stage calls.  The copies of
+    # neighbouring steps are pipelined on two copy streams: step t+1's gradient goes up
+    # while step t orthogonalizes, step t's weights go down while step t+1 starts.
     e2e = None
     if not args.no_e2e:
         need = 2 * 4 * N
         if _mem_available_bytes() > 3 * need:
+            saved_affinity = os.sched_getaffinity(0)
+            _pin_to_gpu_numa_node(dev)
             G_h = torch.empty(N, dtype=torch.float32, pin_memory=True)
             W_h = torch.empty(N, dtype=torch.float32, pin_memory=True)
             G_h.copy_(Gb[:N])
+            os.sched_setaffinity(0, saved_affinity)
+            G2b = torch.empty_like(Gb)
+            gbufs = [Gb, G2b]
+            h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+            comp = torch.cuda.current_stream()
+            n_e2e = max(2, args.steps)
+            ev = lambda: torch.cuda.Event()  # noqa: E731
+            ev_in = [ev(), ev()]
+            ev_k1 = [ev(), ev()]
+            ev_apply = [ev() for _ in range(n_e2e)]
+            ev_out = [ev() for _ in range(n_e2e)]
             torch.cuda.synchronize()
-
-            def e2e_step():
-                Gb[:N].copy_(G_h, non_blocking=True)
-                capi.muon_step(W, G, M, lay, ws, wl.lr, wl.wd, wl.mu, wl.nesterov, ns_steps)
-                W_h.copy_(Wb[:N], non_blocking=True)
-
-            e2e_step()
-            torch.cuda.synchronize()
+            barrier()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
-            barrier()
-            a.record()
-            n_e2e = max(1, min(args.steps, 3))
-            for _ in range(n_e2e):
-                e2e_step()
-            b.record()
+            a.record(comp)
+            h2d.wait_stream(comp)
+            with torch.cuda.stream(h2d):
+                gbufs[0][:N].copy_(G_h, non_blocking=True)
+                ev_in[0].record(h2d)
+            for t in range(n_e2e):
+                cur = gbufs[t % 2]
+                shards = [cur[s * L:(s + 1) * L] for s in range(S)]
+                comp.wait_event(ev_in[t % 2])
+                capi.muon_compute_momentum_inputs(shards, M, lay, ws, wl.mu, wl.nesterov)
+                ev_k1[t % 2].record(comp)
+                if t + 1 < n_e2e:
+                    with torch.cuda.stream(h2d):
+                        if t >= 1:
+                            h2d.wait_event(ev_k1[(t + 1) % 2])
+                        gbufs[(t + 1) % 2][:N].copy_(G_h, non_blocking=True)
+                        ev_in[(t + 1) % 2].record(h2d)
+                capi.muon_orthogonalize_updates(lay, ws, ns_steps)
+                if t >= 1:
+                    comp.wait_event(ev_out[t - 1])
+                capi.muon_apply_local_updates(W, lay, ws, wl.lr, wl.wd, ns_steps)
+                ev_apply[t].record(comp)
+                with torch.cuda.stream(d2h):
+                    d2h.wait_event(ev_apply[t])
+                    W_h.copy_(Wb[:N], non_blocking=True)
+                    ev_out[t].record(d2h)
+            comp.wait_event(ev_out[n_e2e - 1])
+            b.record(comp)
             torch.cuda.synchronize()
             e2e_ms = a.elapsed_time(b) / n_e2e
             if dist is not None:
-                t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-                dist.all_reduce(t, op=dist.ReduceOp.MAX)
-                e2e_ms = float(t[0])
+                t_ = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+                dist.all_reduce(t_, op=dist.ReduceOp.MAX)
+                e2e_ms = float(t_[0])
             e2e = {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": 4 * N,
-                   "d2h_bytes_per_step": 4 * N,
-                   "note": "muon_step with the gradient copied in from pinned host memory and "
-                           "the updated weights copied back, every step"}
-            del G_h, W_h
+                   "d2h_bytes_per_step": 4 * N, "steps": n_e2e,
+                   "note": "per step: gradient H2D from pinned host memory, the three stage "
+                           "calls, updated weights D2H to pinned host memory; copies of "
+                           "neighbouring steps overlap compute on two copy streams"}
+            del G_h, W_h, G2b
         else:
             e2e = {"value": None, "unit": "ms", "h2d_bytes_per_step": 4 * N,
                    "d2h_bytes_per_step": 4 * N,
@@ -357,7 +447,15 @@ def run_ours(args):
     ns_tflops = sym / (ns_ms * 1e-3) / 1e12
     ew_ms = stage_ms[0] + stage_ms[2]
     ew_gbs = (b1 + b3) / (ew_ms * 1e-3) / 1e9
-    peak_tc = peaks["bf16_tflops_sustained"]
+    if args.ns_dtype == "bf16":
+        peak_tc = peaks["bf16_tflops_sustained"]
+        peak_note = "%s bf16 sustained (cuBLAS loop under the power cap)" % peaks["source"]
+    else:
+        # fp32 FMA issue rate: 128 FP32 lanes per SM x 2 flops x SMs x max SM clock.
+        props = torch.cuda.get_device_properties(dev)
+        peak_tc = props.multi_processor_count * 128 * 2 * 2070e6 / 1e12
+        peak_note = "derived fp32 CUDA-core peak: %d SMs x 128 lanes x 2 flops x 2070 MHz" % (
+            props.multi_processor_count)
     launches_per_step = (2 + 3 * ns_steps + 1) if n_mat_elems else 0
     line = {
         "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
@@ -375,10 +473,13 @@ def run_ours(args):
         "stage_ms": {"momentum_inputs": stage_ms[0], "orthogonalize": stage_ms[1],
                      "apply": stage_ms[2]},
         "roofline": {"bound": "tensor" if args.ns_dtype == "bf16" else "alu",
-                     "kernel": "ns_phase_tc_kernel (15 launches per step)",
+                     "kernel": "tcgen05 Newton-Schulz phase kernels (3 per iteration, "
+                               "%d launches per step)" % (3 * ns_steps),
                      "achieved": ns_tflops, "peak": peak_tc, "unit": "TFLOP/s",
-                     "frac": ns_tflops / peak_tc, "traffic": None,
-                     "peak_note": "%s bf16 sustained (cuBLAS loop under the power cap)" % peaks["source"]},
+                     "frac": ns_tflops / peak_tc,
+                     "traffic": ns_traffic(wl.name, args.ns_dtype),
+                     "traffic_unit": "DRAM bytes per launch (ncu, mean over phases)",
+                     "peak_note": peak_note},
         "roofline_elementwise": {"bound": "hbm", "achieved": ew_gbs, "peak": peaks["hbm_gbs"],
                                  "unit": "GB/s", "frac": ew_gbs / peaks["hbm_gbs"],
                                  "bytes_per_step": b1 + b3,

@@ -152,8 +152,17 @@ TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_s
     else if (phase == kPhasePoly) { M = N = m.m; K = m.m; sym = true; }
     else { M = m.rows; N = m.cols; K = m.m; sym = false; }
     const int kb = (K + bk - 1) / bk;
-    for (int i0 = 0; i0 < M; i0 += bm) {
-      for (int j0 = 0; j0 < N; j0 += bn) {
+    // Tile order = the order in which a wave of CTAs picks tiles up (equal-cost tiles are
+    // dealt round-robin).  The Update of a wide matrix (B X: X panels along j, B m x m)
+    // walks j in the outer loop so that each X column panel is read from HBM once while
+    // B stays in L2; every other phase walks rows (i) outermost, which for a tall Update
+    // (X B) streams each X row panel once against the L2-resident B.
+    const bool j_outer = phase == kPhaseUpdate && !m.tall;
+    const int outer = j_outer ? N : M, inner = j_outer ? M : N;
+    const int ostep = j_outer ? bn : bm, istep = j_outer ? bm : bn;
+    for (int o0 = 0; o0 < outer; o0 += ostep) {
+      for (int n0 = 0; n0 < inner; n0 += istep) {
+        const int i0 = j_outer ? n0 : o0, j0 = j_outer ? o0 : n0;
         // Symmetric outputs: only tiles that reach the upper triangle (col >= row).
         if (sym && j0 + bn - 1 < i0) continue;
         Item it;
