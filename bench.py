@@ -310,18 +310,17 @@ def run_ours(args):
     ws = capi.workspace_tensor(lay, dev)
     torch.cuda.synchronize()
 
+    # One timed step = the two calls muon_step makes (stage 1, then stages 2+3 with the
+    # apply fused into the last Newton-Schulz Update), with events between them.
     def step_stages(evs=None):
         if evs is not None:
             evs[0].record()
         capi.muon_compute_momentum_inputs(G, M, lay, ws, wl.mu, wl.nesterov)
         if evs is not None:
             evs[1].record()
-        capi.muon_orthogonalize_updates(lay, ws, ns_steps)
+        capi.muon_orthogonalize_apply(W, lay, ws, wl.lr, wl.wd, ns_steps)
         if evs is not None:
             evs[2].record()
-        capi.muon_apply_local_updates(W, lay, ws, wl.lr, wl.wd, ns_steps)
-        if evs is not None:
-            evs[3].record()
 
     for _ in range(args.warmup):
         step_stages()
@@ -331,7 +330,7 @@ def run_ours(args):
         if dist is not None:
             dist.barrier()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -349,9 +348,9 @@ def run_ours(args):
     barrier()
     capi.muon_check()
     total_ms = t_start.elapsed_time(t_end)
-    stage_ms = [0.0, 0.0, 0.0]
+    stage_ms = [0.0, 0.0]
     for e in evs:
-        for j in range(3):
+        for j in range(2):
             stage_ms[j] += e[j].elapsed_time(e[j + 1])
     stage_ms = [x / args.steps for x in stage_ms]
     if dist is not None:
@@ -443,10 +442,11 @@ def run_ours(args):
     sym, dense = ns_flops(wl.shapes, wl.is_matrix, ns_steps)
     n_mat_elems = sum(r * c for (r, c), f in zip(wl.shapes, wl.is_matrix) if f)
     b1, b3 = elementwise_bytes(n_mat_elems, args.ns_dtype)
+    fused_tail = args.ns_dtype == "bf16" and ns_steps >= 1
     ns_ms = stage_ms[1]
     ns_tflops = sym / (ns_ms * 1e-3) / 1e12
-    ew_ms = stage_ms[0] + stage_ms[2]
-    ew_gbs = (b1 + b3) / (ew_ms * 1e-3) / 1e9
+    ew_ms = stage_ms[0]
+    ew_gbs = b1 / (ew_ms * 1e-3) / 1e9
     if args.ns_dtype == "bf16":
         peak_tc = peaks["bf16_tflops_sustained"]
         peak_note = "%s bf16 sustained (cuBLAS loop under the power cap)" % peaks["source"]
@@ -456,7 +456,8 @@ def run_ours(args):
         peak_tc = props.multi_processor_count * 128 * 2 * 2070e6 / 1e12
         peak_note = "derived fp32 CUDA-core peak: %d SMs x 128 lanes x 2 flops x 2070 MHz" % (
             props.multi_processor_count)
-    launches_per_step = (2 + 3 * ns_steps + 1) if n_mat_elems else 0
+    launches_per_step = (2 + 3 * ns_steps + (0 if (args.ns_dtype == "bf16" and ns_steps >= 1)
+                                             else 1)) if n_mat_elems else 0
     line = {
         "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
@@ -470,21 +471,21 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (%.1f GB per fp32 buffer); no flush" % (4 * N / 1e9)},
         "ns_ms": ns_ms, "ns_tflops": ns_tflops, "ns_tflops_dense_equiv": dense / (ns_ms * 1e-3) / 1e12,
         "ns_flops_sym": sym, "matrices_per_s": wl.n_matrices / (ms * 1e-3),
-        "stage_ms": {"momentum_inputs": stage_ms[0], "orthogonalize": stage_ms[1],
-                     "apply": stage_ms[2]},
+        "stage_ms": {"momentum_inputs": stage_ms[0], "orthogonalize_apply": stage_ms[1]},
+        "fused_apply": fused_tail,
         "roofline": {"bound": "tensor" if args.ns_dtype == "bf16" else "alu",
                      "kernel": "tcgen05 Newton-Schulz phase kernels (3 per iteration, "
-                               "%d launches per step)" % (3 * ns_steps),
+                               "%d launches per step; the last one also applies the "
+                               "update to W)" % (3 * ns_steps),
                      "achieved": ns_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": ns_tflops / peak_tc,
                      "traffic": ns_traffic(wl.name, args.ns_dtype),
                      "traffic_unit": "DRAM bytes per launch (ncu, mean over phases)",
                      "peak_note": peak_note},
-        "roofline_elementwise": {"bound": "hbm", "achieved": ew_gbs, "peak": peaks["hbm_gbs"],
+        "roofline_elementwise": {"bound": "hbm", "kernel": "momentum_input_kernel",
+                                 "achieved": ew_gbs, "peak": peaks["hbm_gbs"],
                                  "unit": "GB/s", "frac": ew_gbs / peaks["hbm_gbs"],
-                                 "bytes_per_step": b1 + b3,
-                                 "stage1_gbs": b1 / (stage_ms[0] * 1e-3) / 1e9,
-                                 "stage3_gbs": b3 / (stage_ms[2] * 1e-3) / 1e9},
+                                 "bytes_per_step": b1},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "e2e": e2e,

@@ -101,7 +101,8 @@ muon_status muon_full_offsets(const muon_layout* layout, int64_t* offsets);
 
 /* ---------------------------------------------------------------- the optimizer step
  * muon_step: one optimizer step over the whole layout ([P2] FsdpMuon.step/_step_group;
- * [P1] "Opt step" 1-6 with the owner emulated on this GPU as indexing):
+ * [P1] "Opt step" 1-6 with the owner emulated on this GPU as indexing); it runs
+ * muon_compute_momentum_inputs then muon_orthogonalize_apply:
  *   1. M <- mu*M + G and the orthogonalization input X = G + mu*M (nesterov != 0) or M,
  *      written straight into per-matrix full matrices in the workspace (the gather);
  *   2. per matrix, Newton-Schulz for ns_steps (0..100) iterations;
@@ -128,6 +129,15 @@ muon_status muon_orthogonalize_updates(const muon_layout* layout, void* workspac
 /* [P2] _apply_local_updates: decay + scaled update into the parameter shards (scatter).
  * ns_steps must match the value given to muon_orthogonalize_updates. */
 muon_status muon_apply_local_updates(float* const* flat_params, const muon_layout* layout,
+                                     void* workspace, float lr, float wd, int32_t ns_steps,
+                                     cudaStream_t stream);
+
+/* Stages 2 and 3 in one call (what muon_step runs after stage 1).  On a bf16 layout with
+ * ns_steps >= 1 the last Newton-Schulz Update applies W <- W*(1 - lr*wd) - lr*scale*O in
+ * its epilogue, from the fp32 O before it is rounded to bf16, and the separate apply pass
+ * is skipped; otherwise it equals muon_orthogonalize_updates + muon_apply_local_updates.
+ * The bf16 O is still stored, so muon_export_update stays valid. */
+muon_status muon_orthogonalize_apply(float* const* flat_params, const muon_layout* layout,
                                      void* workspace, float lr, float wd, int32_t ns_steps,
                                      cudaStream_t stream);
 

@@ -50,6 +50,7 @@ SIGNATURES = [
     ("muon_compute_momentum_inputs", _I32, [_PP, _PP, _P, _P, _F, _I32, _P]),
     ("muon_orthogonalize_updates", _I32, [_P, _P, _I32, _P]),
     ("muon_apply_local_updates", _I32, [_PP, _P, _P, _F, _F, _I32, _P]),
+    ("muon_orthogonalize_apply", _I32, [_PP, _P, _P, _F, _F, _I32, _P]),
     ("muon_gather_full", _I32, [_P, _PP, _P, _P]),
     ("muon_scatter_updates", _I32, [_P, _P, _PP, _P]),
     ("muon_orthogonalize_full", _I32, [_P, _P, _P, _P, _I32, _P]),
@@ -223,6 +224,13 @@ def muon_apply_local_updates(flat_params, layout, workspace, lr, wd, ns_steps=5,
                                         layout.handle, _ptr(workspace), float(lr), float(wd),
                                         int(ns_steps), _stream_handle(stream)),
            "muon_apply_local_updates")
+
+
+def muon_orthogonalize_apply(flat_params, layout, workspace, lr, wd, ns_steps=5, stream=None):
+    _check(lib.muon_orthogonalize_apply(_shard_array(layout, flat_params, "flat_params"),
+                                        layout.handle, _ptr(workspace), float(lr), float(wd),
+                                        int(ns_steps), _stream_handle(stream)),
+           "muon_orthogonalize_apply")
 
 
 def muon_gather_full(layout, shards, full, stream=None):

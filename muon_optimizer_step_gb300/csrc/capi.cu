@@ -242,23 +242,30 @@ muon_status run_momentum(muon_layout* L, const ShardPtrs& g, const ShardPtrs& m,
   return MUON_OK;
 }
 
-muon_status run_ns(muon_layout* L, void* ws, int ns_steps, cudaStream_t st) {
+muon_status run_ns(muon_layout* L, void* ws, int ns_steps, const ApplyArgs* ap, cudaStream_t st) {
   for (int it = 0; it < ns_steps; ++it) {
     const int x_in = it & 1;
     const int iter0 = it == 0 ? 1 : 0;
     for (int ph = 0; ph < 3; ++ph) {
+      const ApplyArgs* fuse = (ph == kPhaseUpdate && it == ns_steps - 1) ? ap : nullptr;
       cudaError_t e;
       if (L->plan.ns_dtype != MUON_NS_BF16)
         e = launch_ns_phase_f32(L->plan, L->dt, ws, ph, x_in, iter0, st);
       else if (L->dt.tc_variant[ph] == 2)
-        e = launch_ns_phase_tc2(L->plan, L->dt, ws, ph, x_in, iter0, kDefaultBudget, st);
+        e = launch_ns_phase_tc2(L->plan, L->dt, ws, ph, x_in, iter0, kDefaultBudget, fuse, st);
       else
-        e = launch_ns_phase_tc(L->plan, L->dt, ws, ph, x_in, iter0, kDefaultBudget, st);
+        e = launch_ns_phase_tc(L->plan, L->dt, ws, ph, x_in, iter0, kDefaultBudget, fuse, st);
       if (e != cudaSuccess) return cuda_fail(e, "newton_schulz phase");
     }
   }
   return MUON_OK;
 }
+
+// Stages 2 and 3.  On the tensor-core path with at least one iteration the last Update's
+// epilogue applies W <- W*(1 - lr*wd) - lr*scale*O itself, from the fp32 O, and the
+// separate apply pass is skipped.
+muon_status run_ns_apply(muon_layout* L, const ShardPtrs& w, void* ws, float lr, float wd,
+                         int ns_steps, cudaStream_t st);
 
 muon_status run_apply(muon_layout* L, const ShardPtrs& w, void* ws, float lr, float wd,
                       int ns_steps, cudaStream_t st) {
@@ -266,6 +273,21 @@ muon_status run_apply(muon_layout* L, const ShardPtrs& w, void* ws, float lr, fl
   MUON_CUDA(launch_apply(L->plan, L->dt, w, ws, ns_steps & 1, ns_steps == 0 ? 1 : 0, decay, lr, st),
             "apply");
   return MUON_OK;
+}
+
+muon_status run_ns_apply(muon_layout* L, const ShardPtrs& w, void* ws, float lr, float wd,
+                         int ns_steps, cudaStream_t st) {
+  if (L->plan.ns_dtype == MUON_NS_BF16 && ns_steps >= 1) {
+    ApplyArgs ap;
+    ap.W = w;
+    ap.L = L->plan.L;
+    ap.decay = (float)(1.0 - (double)lr * (double)wd);
+    ap.lr = lr;
+    return run_ns(L, ws, ns_steps, &ap, st);
+  }
+  muon_status s = run_ns(L, ws, ns_steps, nullptr, st);
+  if (s != MUON_OK) return s;
+  return run_apply(L, w, ws, lr, wd, ns_steps, st);
 }
 
 muon_status check_scalars(float lr, float wd, float mu) {
@@ -369,7 +391,24 @@ muon_status muon_orthogonalize_updates(const muon_layout* layout, void* workspac
   std::lock_guard<std::mutex> guard(L->mu);
   MUON_TRY(ensure_device(L));
   MUON_TRY(ensure_tmaps(L, workspace));
-  MUON_TRY(run_ns(L, workspace, ns_steps, stream));
+  MUON_TRY(run_ns(L, workspace, ns_steps, nullptr, stream));
+  return ok();
+}
+
+muon_status muon_orthogonalize_apply(float* const* flat_params, const muon_layout* layout,
+                                     void* workspace, float lr, float wd, int32_t ns_steps,
+                                     cudaStream_t stream) {
+  if (layout == nullptr) return fail(MUON_ERR_INVALID_ARG, "layout is NULL");
+  muon_layout* L = const_cast<muon_layout*>(layout);
+  ShardPtrs w;
+  MUON_TRY(check_shards(L, reinterpret_cast<const void* const*>(flat_params), "flat_params", &w));
+  MUON_TRY(check_ws(L, workspace));
+  MUON_TRY(check_steps(ns_steps));
+  MUON_TRY(check_scalars(lr, wd, 0.f));
+  std::lock_guard<std::mutex> guard(L->mu);
+  MUON_TRY(ensure_device(L));
+  MUON_TRY(ensure_tmaps(L, workspace));
+  MUON_TRY(run_ns_apply(L, w, workspace, lr, wd, ns_steps, stream));
   return ok();
 }
 
@@ -406,8 +445,7 @@ muon_status muon_step(float* const* flat_params, const float* const* flat_grads,
   MUON_TRY(ensure_device(L));
   MUON_TRY(ensure_tmaps(L, workspace));
   MUON_TRY(run_momentum(L, g, m, workspace, mu, nesterov != 0, stream));
-  MUON_TRY(run_ns(L, workspace, ns_steps, stream));
-  MUON_TRY(run_apply(L, w, workspace, lr, wd, ns_steps, stream));
+  MUON_TRY(run_ns_apply(L, w, workspace, lr, wd, ns_steps, stream));
   return ok();
 }
 
@@ -452,7 +490,7 @@ muon_status muon_orthogonalize_full(const muon_layout* layout, void* workspace, 
   MUON_TRY(ensure_tmaps(L, workspace));
   MUON_CUDA(launch_full_input(L->plan, L->dt, full_in, workspace, stream), "full_input");
   MUON_CUDA(launch_norm_finalize(L->plan, L->dt, workspace, stream), "norm_finalize");
-  MUON_TRY(run_ns(L, workspace, ns_steps, stream));
+  MUON_TRY(run_ns(L, workspace, ns_steps, nullptr, stream));
   MUON_CUDA(launch_export(L->plan, L->dt, workspace, ns_steps & 1, ns_steps == 0 ? 1 : 0, full_out,
                           stream),
             "export");

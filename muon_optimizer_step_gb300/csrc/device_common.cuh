@@ -248,6 +248,90 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t mask) {
       : "memory");
 }
 
+// ------------------------------------------------------------------ fused apply
+// Arguments of the last Newton-Schulz Update when it also applies the step to the weights.
+struct ApplyArgs {
+  ShardPtrs W;     // parameter shards
+  long long L;     // shard length
+  float decay;     // 1 - lr * wd
+  float lr;
+};
+
+// W <- W * decay - lr * scale * O for the elements (i, jb .. jb + n - 1) of a matrix, whose
+// row-major element (i, j) lives at flat index flat_off + i * cols + j of the sharded
+// buffer.  o holds the fp32 update values.  128-bit accesses when the run lies in one
+// shard and is aligned, element by element otherwise.
+__device__ __forceinline__ void apply_row_run(const ApplyArgs& ap, const MatDev& mt, int i, int jb,
+                                              int n, const float (&o)[32]) {
+  const float lrs = ap.lr * mt.scale;
+  const long long g0 = mt.flat_off + (long long)i * mt.cols + jb;
+  const long long s0 = g0 / ap.L;
+  const long long off0 = g0 - s0 * ap.L;
+  if (n == 32 && off0 + 32 <= ap.L && (off0 & 3) == 0) {
+    float4* w = reinterpret_cast<float4*>(ap.W.p[s0] + off0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float4 v = w[q];
+      v.x = fmaf(-lrs, o[4 * q + 0], v.x * ap.decay);
+      v.y = fmaf(-lrs, o[4 * q + 1], v.y * ap.decay);
+      v.z = fmaf(-lrs, o[4 * q + 2], v.z * ap.decay);
+      v.w = fmaf(-lrs, o[4 * q + 3], v.w * ap.decay);
+      w[q] = v;
+    }
+  } else {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      if (t < n) {
+        const long long g = g0 + t;
+        const long long s = g / ap.L;
+        float* w = ap.W.p[s] + (g - s * ap.L);
+        *w = fmaf(-lrs, o[t], *w * ap.decay);
+      }
+    }
+  }
+}
+
+// Two-part form of apply_row_run for a full run of 32: load the weights first (returns
+// whether the 128-bit path applies), store them updated later.
+__device__ __forceinline__ bool apply_load_row_run(const ApplyArgs& ap, const MatDev& mt, int i,
+                                                   int jb, float (&w)[32]) {
+  const long long g0 = mt.flat_off + (long long)i * mt.cols + jb;
+  const long long s0 = g0 / ap.L;
+  const long long off0 = g0 - s0 * ap.L;
+  if (off0 + 32 <= ap.L && (off0 & 3) == 0) {
+    const float4* src = reinterpret_cast<const float4*>(ap.W.p[s0] + off0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 v = src[q];
+      w[4 * q + 0] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+    }
+    return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void apply_store_row_run(const ApplyArgs& ap, const MatDev& mt, int i,
+                                                    int jb, bool vec, const float (&w)[32],
+                                                    const float (&o)[32]) {
+  if (!vec) {
+    apply_row_run(ap, mt, i, jb, 32, o);
+    return;
+  }
+  const float lrs = ap.lr * mt.scale;
+  const long long g0 = mt.flat_off + (long long)i * mt.cols + jb;
+  const long long s0 = g0 / ap.L;
+  float4* dst = reinterpret_cast<float4*>(ap.W.p[s0] + (g0 - s0 * ap.L));
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    float4 v;
+    v.x = fmaf(-lrs, o[4 * q + 0], w[4 * q + 0] * ap.decay);
+    v.y = fmaf(-lrs, o[4 * q + 1], w[4 * q + 1] * ap.decay);
+    v.z = fmaf(-lrs, o[4 * q + 2], w[4 * q + 2] * ap.decay);
+    v.w = fmaf(-lrs, o[4 * q + 3], w[4 * q + 3] * ap.decay);
+    dst[q] = v;
+  }
+}
+
 // ------------------------------------------------------------------ small math helpers
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

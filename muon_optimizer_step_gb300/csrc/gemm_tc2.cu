@@ -38,7 +38,8 @@ constexpr int A_BYTES = HM * BK * 2;            // 16 KB
 constexpr int B_BYTES = HM * BK * 2;            // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB per CTA
 constexpr int MN_BOX_BYTES = 64 * BK * 2;       // 8 KB
-constexpr int NUM_THREADS = 256;
+constexpr int NUM_THREADS = 384;  // warps 0-3 roles, warps 4-11 epilogue
+constexpr int EPI_WARPS = 8;
 constexpr int TMEM_COLS = 512;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr float kA = 3.4445f, kB = -4.7750f, kC = 2.0315f;
@@ -55,6 +56,8 @@ struct Tc2Params {
   int phase;
   int x_in;
   int iter0;
+  int apply;        // last Update: also W <- W*decay - lr*scale*O (fp32 O)
+  ApplyArgs ap;
 };
 
 struct TileOps {
@@ -116,6 +119,17 @@ __device__ __forceinline__ void epilogue_chunk(const Tc2Params& p, const MatDev&
     if (jb + 32 <= mt.cols) {
       float x[32];
       load_bf16x32(xin + row + jb, x);
+      if (p.apply) {
+        // Issue the weight loads with the X loads, before any store, so that the two
+        // memory round trips of this chunk overlap.
+        float w[32];
+        const bool vec = apply_load_row_run(p.ap, mt, i, jb, w);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) f[t] = s * fmaf(kA, x[t], __uint_as_float(acc[t]));
+        store_bf16x32(xout + row + jb, f);
+        apply_store_row_run(p.ap, mt, i, jb, vec, w, f);
+        return;
+      }
 #pragma unroll
       for (int t = 0; t < 32; ++t) f[t] = s * fmaf(kA, x[t], __uint_as_float(acc[t]));
       store_bf16x32(xout + row + jb, f);
@@ -123,11 +137,14 @@ __device__ __forceinline__ void epilogue_chunk(const Tc2Params& p, const MatDev&
 #pragma unroll
       for (int t = 0; t < 32; ++t) {
         const int j = jb + t;
-        if (j < mt.cols)
-          xout[row + j] = __float2bfloat16_rn(
-              s * fmaf(kA, __bfloat162float(xin[row + j]), __uint_as_float(acc[t])));
+        f[t] = 0.f;
+        if (j < mt.cols) {
+          f[t] = s * fmaf(kA, __bfloat162float(xin[row + j]), __uint_as_float(acc[t]));
+          xout[row + j] = __float2bfloat16_rn(f[t]);
+        }
       }
     }
+    if (p.apply) apply_row_run(p.ap, mt, i, jb, min(32, mt.cols - jb), f);
     return;
   }
   if (i >= mt.m || jb + 31 < i || jb >= mt.m) return;
@@ -188,7 +205,7 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, long 
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    ns_phase_tc2_kernel(const Tc2Params p) {
+    ns_phase_tc2_kernel(const __grid_constant__ Tc2Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -214,7 +231,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 2 * 4);  // one arrival per epilogue warp of the pair
+      mbar_init(&acc_empty[b], 2 * EPI_WARPS);  // one arrival per epilogue warp of the pair
     }
     mbar_init(mma_done, 1);
     abort_flag = 0;
@@ -333,7 +350,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue (both CTAs)
-    const int q = warp - 4;
+    // Two epilogue warps per TMEM lane quarter (warp % 4), each draining half the columns.
+    const int q = warp & 3;
+    const int half = (warp - 4) >> 2;
     const int r = 32 * q + lane;
     int lt = 0;
     for (int ti = t_begin; ti < t_end; ++ti, ++lt) {
@@ -355,7 +374,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       }
       const int i = tile.i0 + HM * (int)rank + r;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * BN + 32 * c),
                            v);
@@ -396,7 +415,8 @@ cudaError_t prepare_tc2_kernel(int* max_pairs) {
 }
 
 cudaError_t launch_ns_phase_tc2(const Plan& plan, const DevTables& dt, void* ws, int phase,
-                                int x_in, int iter0, long long budget, cudaStream_t st) {
+                                int x_in, int iter0, long long budget, const ApplyArgs* ap,
+                                cudaStream_t st) {
   const int pairs = dt.grid[phase];
   if (pairs == 0) return cudaSuccess;
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -412,6 +432,8 @@ cudaError_t launch_ns_phase_tc2(const Plan& plan, const DevTables& dt, void* ws,
   p.phase = phase;
   p.x_in = x_in;
   p.iter0 = iter0;
+  p.apply = ap != nullptr ? 1 : 0;
+  if (ap != nullptr) p.ap = *ap;
   ns_phase_tc2_kernel<<<2 * pairs, NUM_THREADS, SMEM_BYTES, st>>>(p);
   return cudaGetLastError();
 }

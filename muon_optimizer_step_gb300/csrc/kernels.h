@@ -11,6 +11,7 @@
 namespace muon {
 
 struct ShardPtrs;
+struct ApplyArgs;
 
 // Device-resident tables of a layout (uploaded once per device).
 struct DevTables {
@@ -52,11 +53,14 @@ cudaError_t launch_export(const Plan& plan, const DevTables& dt, const void* ws,
                           int pending_norm, float* full, cudaStream_t st);
 
 // Stage 2, bf16 path: one tcgen05 GEMM phase over every matrix.
+// With ap != nullptr (last Update only) the epilogue also applies the step to the weights.
 cudaError_t launch_ns_phase_tc(const Plan& plan, const DevTables& dt, void* ws, int phase,
-                               int x_in, int iter0, long long budget, cudaStream_t st);
+                               int x_in, int iter0, long long budget, const ApplyArgs* ap,
+                               cudaStream_t st);
 // Stage 2, bf16 path on CTA pairs (tcgen05 cta_group::2): grid[phase] counts pairs.
 cudaError_t launch_ns_phase_tc2(const Plan& plan, const DevTables& dt, void* ws, int phase,
-                                int x_in, int iter0, long long budget, cudaStream_t st);
+                                int x_in, int iter0, long long budget, const ApplyArgs* ap,
+                                cudaStream_t st);
 // Shared-memory opt-in of the pair kernel and how many pairs can be resident at once.
 cudaError_t prepare_tc2_kernel(int* max_pairs);
 // Stage 2, fp32 path: one SIMT GEMM phase over every matrix.

@@ -45,7 +45,7 @@ struct ChunkDev {          // 32 bytes
   int32_t vec;             // 1: inside one shard, and offsets allow 128-bit accesses
 };
 
-struct MatDev {            // 96 bytes
+struct MatDev {            // 104 bytes
   int32_t rows, cols;      // stored shape
   int32_t m, n;            // min / max of (rows, cols)
   int32_t tall;            // rows > cols: work on X^T (A = X^T X, X' = aX + X B)
@@ -58,6 +58,7 @@ struct MatDev {            // 96 bytes
   int64_t chunk_end;
   float scale;             // sqrt(max(1, rows/cols))
   float pad_;
+  int64_t flat_off;        // element offset of the matrix in the unsharded flat buffer
 };
 
 struct TileDev {           // 16 bytes: one output tile of one GEMM phase

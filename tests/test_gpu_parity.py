@@ -244,28 +244,53 @@ def test_ragged_two_steps(capi, ns_dtype, n_shards):
 
 @pytest.mark.parametrize("ns_dtype", [0, 1])
 def test_step_equals_stages_and_sharding_is_exact(capi, ns_dtype):
-    """muon_step = the three stage calls, bit for bit; 1 shard vs 5 shards bit for bit."""
+    """muon_step = stage 1 + muon_orthogonalize_apply, bit for bit; 1 vs 5 shards bit for
+    bit; and against the three separate stages: equal on the fp32 path, and on the bf16
+    path (whose fused tail applies the fp32 O instead of its bf16 rounding) within the
+    rounding of two steps' O: sum_t lr * scale * 2^-9 * ||O_t|| <= lr * scale * 2^-7 * ||O_2||
+    (the two steps' updates have nearly equal norms)."""
     wl = inputs.WORKLOADS["ragged_small"]
     W0, Gs, M0 = inputs.host_inputs(wl)
     results = []
-    for n_shards, fused in [(1, True), (5, True), (5, False)]:
+    O_last = None
+    for n_shards, mode in [(1, "step"), (5, "step"), (5, "fused"), (5, "stages")]:
         lay = capi.muon_layout_create(wl.shapes, n_shards, ns_dtype, wl.is_matrix)
         ws = capi.workspace_tensor(lay)
         W = split_shards(W0, n_shards)
         M = split_shards(M0, n_shards)
         for t in range(2):
             G = split_shards(Gs[t], n_shards)
-            if fused:
+            if mode == "step":
                 capi.muon_step(W, G, M, lay, ws, wl.lr, wl.wd, wl.mu, True, 5)
             else:
                 capi.muon_compute_momentum_inputs(G, M, lay, ws, wl.mu, True)
-                capi.muon_orthogonalize_updates(lay, ws, 5)
-                capi.muon_apply_local_updates(W, lay, ws, wl.lr, wl.wd, 5)
+                if mode == "fused":
+                    capi.muon_orthogonalize_apply(W, lay, ws, wl.lr, wl.wd, 5)
+                else:
+                    capi.muon_orthogonalize_updates(lay, ws, 5)
+                    capi.muon_apply_local_updates(W, lay, ws, wl.lr, wl.wd, 5)
+        if mode == "stages":
+            O_last = torch.zeros(lay.full_numel, device="cuda")
+            capi.muon_export_update(lay, ws, 5, O_last)
         capi.muon_check()
         results.append((join_shards(W, lay.numel), join_shards(M, lay.numel)))
-    for Wr, Mr in results[1:]:
+    for Wr, Mr in results[1:3]:
         assert np.array_equal(Wr, results[0][0])
         assert np.array_equal(Mr, results[0][1])
+    W_st, M_st = results[3]
+    assert np.array_equal(M_st, results[0][1])
+    if ns_dtype == 1:
+        assert np.array_equal(W_st, results[0][0])
+        return
+    o = ref.flat_layout(wl.shapes, 1, wl.is_matrix)
+    O = full_to_mats(O_last, capi.muon_layout_create(wl.shapes, 1, 0, wl.is_matrix), wl)
+    for i, Oi in O.items():
+        r, c = wl.shapes[i]
+        sl = slice(o["offsets"][i], o["offsets"][i] + r * c)
+        bound = wl.lr * ref.update_scale(r, c) * 2.0 ** -7 * np.linalg.norm(Oi) \
+            + 1e-6 * np.linalg.norm(W_st[sl].astype(np.float64))
+        diff = np.linalg.norm(results[0][0][sl].astype(np.float64) - W_st[sl])
+        assert diff <= bound, (i, diff, bound)
 
 
 def test_repeat_runs_are_bit_identical(capi):
