@@ -117,6 +117,31 @@ muon_status muon_step(float* const* flat_params, const float* const* flat_grads,
                       float lr, float wd, float mu, int32_t nesterov, int32_t ns_steps,
                       cudaStream_t stream);
 
+/* ---------------------------------------------------------------- optimizer groups
+ * [P2] _FsdpGroupAssignment.tensor_to_optimizer_group_index maps each tensor of an FSDP
+ * group to an optimizer group (its own lr, weight decay, momentum).  The grouping is a
+ * property of the layout; the groups' values come with every call.
+ * muon_layout_set_groups: group_of[i] in 0..n_groups-1 for every matrix parameter i (host
+ * array of n_params entries; entries of non-matrix parameters are ignored), 1 <= n_groups
+ * <= 32.  All matrices start in group 0.  If the layout's tables are already on the GPU
+ * they are refreshed synchronously; do not call it while a step of this layout runs. */
+muon_status muon_layout_set_groups(muon_layout* layout, const int32_t* group_of,
+                                   int32_t n_groups);
+
+typedef struct muon_group_hparams {
+  float lr;          /* learning rate */
+  float wd;          /* decoupled weight decay (the factor is 1 - lr*wd) */
+  float mu;          /* momentum coefficient */
+  int32_t nesterov;  /* nonzero: orthogonalize G + mu*M, else M */
+} muon_group_hparams;
+
+/* muon_step with per-group hyper-parameters: groups is a host array of the layout's
+ * n_groups entries; matrix i uses groups[group_of[i]].  Everything else as muon_step. */
+muon_status muon_step_grouped(float* const* flat_params, const float* const* flat_grads,
+                              float* const* flat_momentum, const muon_layout* layout,
+                              void* workspace, const muon_group_hparams* groups, int32_t ns_steps,
+                              cudaStream_t stream);
+
 /* The three stages of muon_step, callable one by one (same arguments, same meaning).
  * [P2] _compute_momentum_inputs: momentum update, input build, gather, Frobenius norms. */
 muon_status muon_compute_momentum_inputs(const float* const* flat_grads,

@@ -35,6 +35,13 @@ _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
 _F = ctypes.c_float
 _PP = ctypes.POINTER(ctypes.c_void_p)
+
+
+class GroupHparams(ctypes.Structure):
+    """muon_group_hparams: one optimizer group's hyper-parameters."""
+    _fields_ = [("lr", ctypes.c_float), ("wd", ctypes.c_float), ("mu", ctypes.c_float),
+                ("nesterov", ctypes.c_int32)]
+
 SIGNATURES = [
     ("muon_abi_version", _I32, []),
     ("muon_last_error", ctypes.c_char_p, []),
@@ -51,6 +58,8 @@ SIGNATURES = [
     ("muon_orthogonalize_updates", _I32, [_P, _P, _I32, _P]),
     ("muon_apply_local_updates", _I32, [_PP, _P, _P, _F, _F, _I32, _P]),
     ("muon_orthogonalize_apply", _I32, [_PP, _P, _P, _F, _F, _I32, _P]),
+    ("muon_layout_set_groups", _I32, [_P, ctypes.POINTER(_I32), _I32]),
+    ("muon_step_grouped", _I32, [_PP, _PP, _PP, _P, _P, ctypes.POINTER(GroupHparams), _I32, _P]),
     ("muon_gather_full", _I32, [_P, _PP, _P, _P]),
     ("muon_scatter_updates", _I32, [_P, _P, _PP, _P]),
     ("muon_orthogonalize_full", _I32, [_P, _P, _P, _P, _I32, _P]),
@@ -204,6 +213,25 @@ def muon_step(flat_params, flat_grads, flat_momentum, layout, workspace, lr, wd,
                          layout.handle, _ptr(workspace), float(lr), float(wd), float(mu),
                          1 if nesterov else 0, int(ns_steps), _stream_handle(stream)),
            "muon_step")
+
+
+def muon_layout_set_groups(layout, group_of, n_groups):
+    arr = (_I32 * max(1, len(group_of)))(*[int(g) for g in group_of])
+    _check(lib.muon_layout_set_groups(layout.handle, arr, int(n_groups)), "muon_layout_set_groups")
+    layout.n_groups = int(n_groups)
+
+
+def muon_step_grouped(flat_params, flat_grads, flat_momentum, layout, workspace, groups,
+                      ns_steps=5, stream=None):
+    """groups: a sequence of (lr, wd, mu, nesterov), one per optimizer group."""
+    arr = (GroupHparams * max(1, len(groups)))(
+        *[GroupHparams(float(lr), float(wd), float(mu), 1 if nest else 0)
+          for lr, wd, mu, nest in groups])
+    _check(lib.muon_step_grouped(_shard_array(layout, flat_params, "flat_params"),
+                                 _shard_array(layout, flat_grads, "flat_grads"),
+                                 _shard_array(layout, flat_momentum, "flat_momentum"),
+                                 layout.handle, _ptr(workspace), arr, int(ns_steps),
+                                 _stream_handle(stream)), "muon_step_grouped")
 
 
 def muon_compute_momentum_inputs(flat_grads, flat_momentum, layout, workspace, mu,

@@ -235,9 +235,22 @@ muon_status check_steps(int32_t ns_steps) {
   } while (0)
 
 // ---- the three stages (arguments already validated, tables ready) ----
+// Hyper-parameters of a call: every group slot holds the same values (ungrouped calls),
+// or one slot per optimizer group.
+GroupParams uniform_groups(float lr, float wd, float mu, int nesterov) {
+  GroupParams gp;
+  for (int k = 0; k < kMaxGroups; ++k) {
+    gp.lr[k] = lr;
+    gp.decay[k] = (float)(1.0 - (double)lr * (double)wd);
+    gp.mu[k] = mu;
+    gp.nesterov[k] = nesterov ? 1 : 0;
+  }
+  return gp;
+}
+
 muon_status run_momentum(muon_layout* L, const ShardPtrs& g, const ShardPtrs& m, void* ws,
-                         float mu, int nesterov, cudaStream_t st) {
-  MUON_CUDA(launch_momentum_input(L->plan, L->dt, g, m, ws, mu, nesterov, st), "momentum_input");
+                         const GroupParams& gp, cudaStream_t st) {
+  MUON_CUDA(launch_momentum_input(L->plan, L->dt, g, m, ws, gp, st), "momentum_input");
   MUON_CUDA(launch_norm_finalize(L->plan, L->dt, ws, st), "norm_finalize");
   return MUON_OK;
 }
@@ -264,30 +277,28 @@ muon_status run_ns(muon_layout* L, void* ws, int ns_steps, const ApplyArgs* ap, 
 // Stages 2 and 3.  On the tensor-core path with at least one iteration the last Update's
 // epilogue applies W <- W*(1 - lr*wd) - lr*scale*O itself, from the fp32 O, and the
 // separate apply pass is skipped.
-muon_status run_ns_apply(muon_layout* L, const ShardPtrs& w, void* ws, float lr, float wd,
+muon_status run_ns_apply(muon_layout* L, const ShardPtrs& w, void* ws, const GroupParams& gp,
                          int ns_steps, cudaStream_t st);
 
-muon_status run_apply(muon_layout* L, const ShardPtrs& w, void* ws, float lr, float wd,
+muon_status run_apply(muon_layout* L, const ShardPtrs& w, void* ws, const GroupParams& gp,
                       int ns_steps, cudaStream_t st) {
-  const float decay = (float)(1.0 - (double)lr * (double)wd);
-  MUON_CUDA(launch_apply(L->plan, L->dt, w, ws, ns_steps & 1, ns_steps == 0 ? 1 : 0, decay, lr, st),
+  MUON_CUDA(launch_apply(L->plan, L->dt, w, ws, ns_steps & 1, ns_steps == 0 ? 1 : 0, gp, st),
             "apply");
   return MUON_OK;
 }
 
-muon_status run_ns_apply(muon_layout* L, const ShardPtrs& w, void* ws, float lr, float wd,
+muon_status run_ns_apply(muon_layout* L, const ShardPtrs& w, void* ws, const GroupParams& gp,
                          int ns_steps, cudaStream_t st) {
   if (L->plan.ns_dtype == MUON_NS_BF16 && ns_steps >= 1) {
     ApplyArgs ap;
     ap.W = w;
     ap.L = L->plan.L;
-    ap.decay = (float)(1.0 - (double)lr * (double)wd);
-    ap.lr = lr;
+    ap.gp = gp;
     return run_ns(L, ws, ns_steps, &ap, st);
   }
   muon_status s = run_ns(L, ws, ns_steps, nullptr, st);
   if (s != MUON_OK) return s;
-  return run_apply(L, w, ws, lr, wd, ns_steps, st);
+  return run_apply(L, w, ws, gp, ns_steps, st);
 }
 
 muon_status check_scalars(float lr, float wd, float mu) {
@@ -378,7 +389,7 @@ muon_status muon_compute_momentum_inputs(const float* const* flat_grads,
   MUON_TRY(check_scalars(0.f, 0.f, mu));
   std::lock_guard<std::mutex> guard(L->mu);
   MUON_TRY(ensure_device(L));
-  MUON_TRY(run_momentum(L, g, m, workspace, mu, nesterov != 0, stream));
+  MUON_TRY(run_momentum(L, g, m, workspace, uniform_groups(0.f, 0.f, mu, nesterov), stream));
   return ok();
 }
 
@@ -408,7 +419,7 @@ muon_status muon_orthogonalize_apply(float* const* flat_params, const muon_layou
   std::lock_guard<std::mutex> guard(L->mu);
   MUON_TRY(ensure_device(L));
   MUON_TRY(ensure_tmaps(L, workspace));
-  MUON_TRY(run_ns_apply(L, w, workspace, lr, wd, ns_steps, stream));
+  MUON_TRY(run_ns_apply(L, w, workspace, uniform_groups(lr, wd, 0.f, 0), ns_steps, stream));
   return ok();
 }
 
@@ -424,7 +435,7 @@ muon_status muon_apply_local_updates(float* const* flat_params, const muon_layou
   MUON_TRY(check_scalars(lr, wd, 0.f));
   std::lock_guard<std::mutex> guard(L->mu);
   MUON_TRY(ensure_device(L));
-  MUON_TRY(run_apply(L, w, workspace, lr, wd, ns_steps, stream));
+  MUON_TRY(run_apply(L, w, workspace, uniform_groups(lr, wd, 0.f, 0), ns_steps, stream));
   return ok();
 }
 
@@ -444,8 +455,66 @@ muon_status muon_step(float* const* flat_params, const float* const* flat_grads,
   std::lock_guard<std::mutex> guard(L->mu);
   MUON_TRY(ensure_device(L));
   MUON_TRY(ensure_tmaps(L, workspace));
-  MUON_TRY(run_momentum(L, g, m, workspace, mu, nesterov != 0, stream));
-  MUON_TRY(run_ns_apply(L, w, workspace, lr, wd, ns_steps, stream));
+  const GroupParams gp = uniform_groups(lr, wd, mu, nesterov);
+  MUON_TRY(run_momentum(L, g, m, workspace, gp, stream));
+  MUON_TRY(run_ns_apply(L, w, workspace, gp, ns_steps, stream));
+  return ok();
+}
+
+muon_status muon_layout_set_groups(muon_layout* layout, const int32_t* group_of,
+                                   int32_t n_groups) {
+  if (layout == nullptr) return fail(MUON_ERR_INVALID_ARG, "layout is NULL");
+  if (n_groups < 1 || n_groups > kMaxGroups)
+    return fail(MUON_ERR_INVALID_ARG, "n_groups=%d outside 1..%d", n_groups, kMaxGroups);
+  if (group_of == nullptr && layout->plan.n_params > 0)
+    return fail(MUON_ERR_INVALID_ARG, "group_of is NULL");
+  for (int32_t i = 0; i < layout->plan.n_params; ++i)
+    if (layout->plan.is_matrix[i] && (group_of[i] < 0 || group_of[i] >= n_groups))
+      return fail(MUON_ERR_INVALID_ARG, "group_of[%d]=%d outside 0..%d", i, group_of[i],
+                  n_groups - 1);
+  std::lock_guard<std::mutex> guard(layout->mu);
+  for (MatDev& m : layout->plan.mats) m.group = group_of[m.param];
+  layout->plan.n_groups = n_groups;
+  if (layout->dt.device >= 0 && !layout->plan.mats.empty()) {
+    // Tables already on the GPU: refresh the matrix records (synchronous).
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != layout->dt.device) cudaSetDevice(layout->dt.device);
+    const cudaError_t e = cudaMemcpy(layout->dt.mats, layout->plan.mats.data(),
+                                     layout->plan.mats.size() * sizeof(MatDev),
+                                     cudaMemcpyHostToDevice);
+    if (cur >= 0 && cur != layout->dt.device) cudaSetDevice(cur);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(matrix records)");
+  }
+  return ok();
+}
+
+muon_status muon_step_grouped(float* const* flat_params, const float* const* flat_grads,
+                              float* const* flat_momentum, const muon_layout* layout,
+                              void* workspace, const muon_group_hparams* groups, int32_t ns_steps,
+                              cudaStream_t stream) {
+  if (layout == nullptr) return fail(MUON_ERR_INVALID_ARG, "layout is NULL");
+  muon_layout* L = const_cast<muon_layout*>(layout);
+  if (groups == nullptr) return fail(MUON_ERR_INVALID_ARG, "groups is NULL");
+  ShardPtrs w, g, m;
+  MUON_TRY(check_shards(L, reinterpret_cast<const void* const*>(flat_params), "flat_params", &w));
+  MUON_TRY(check_shards(L, reinterpret_cast<const void* const*>(flat_grads), "flat_grads", &g));
+  MUON_TRY(check_shards(L, reinterpret_cast<const void* const*>(flat_momentum), "flat_momentum", &m));
+  MUON_TRY(check_ws(L, workspace));
+  MUON_TRY(check_steps(ns_steps));
+  GroupParams gp = uniform_groups(0.f, 0.f, 0.f, 0);
+  for (int k = 0; k < L->plan.n_groups; ++k) {
+    MUON_TRY(check_scalars(groups[k].lr, groups[k].wd, groups[k].mu));
+    gp.lr[k] = groups[k].lr;
+    gp.decay[k] = (float)(1.0 - (double)groups[k].lr * (double)groups[k].wd);
+    gp.mu[k] = groups[k].mu;
+    gp.nesterov[k] = groups[k].nesterov != 0 ? 1 : 0;
+  }
+  std::lock_guard<std::mutex> guard(L->mu);
+  MUON_TRY(ensure_device(L));
+  MUON_TRY(ensure_tmaps(L, workspace));
+  MUON_TRY(run_momentum(L, g, m, workspace, gp, stream));
+  MUON_TRY(run_ns_apply(L, w, workspace, gp, ns_steps, stream));
   return ok();
 }
 

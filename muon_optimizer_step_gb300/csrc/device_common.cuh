@@ -249,12 +249,19 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t mask) {
 }
 
 // ------------------------------------------------------------------ fused apply
+// Per-group hyper-parameters of one call (group g of a matrix = MatDev::group).
+struct GroupParams {
+  float lr[kMaxGroups];
+  float decay[kMaxGroups];  // 1 - lr * wd
+  float mu[kMaxGroups];
+  int nesterov[kMaxGroups];
+};
+
 // Arguments of the last Newton-Schulz Update when it also applies the step to the weights.
 struct ApplyArgs {
   ShardPtrs W;     // parameter shards
   long long L;     // shard length
-  float decay;     // 1 - lr * wd
-  float lr;
+  GroupParams gp;  // lr and decay per group
 };
 
 // W <- W * decay - lr * scale * O for the elements (i, jb .. jb + n - 1) of a matrix, whose
@@ -263,7 +270,8 @@ struct ApplyArgs {
 // shard and is aligned, element by element otherwise.
 __device__ __forceinline__ void apply_row_run(const ApplyArgs& ap, const MatDev& mt, int i, int jb,
                                               int n, const float (&o)[32]) {
-  const float lrs = ap.lr * mt.scale;
+  const float lrs = ap.gp.lr[mt.group] * mt.scale;
+  const float decay = ap.gp.decay[mt.group];
   const long long g0 = mt.flat_off + (long long)i * mt.cols + jb;
   const long long s0 = g0 / ap.L;
   const long long off0 = g0 - s0 * ap.L;
@@ -272,10 +280,10 @@ __device__ __forceinline__ void apply_row_run(const ApplyArgs& ap, const MatDev&
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       float4 v = w[q];
-      v.x = fmaf(-lrs, o[4 * q + 0], v.x * ap.decay);
-      v.y = fmaf(-lrs, o[4 * q + 1], v.y * ap.decay);
-      v.z = fmaf(-lrs, o[4 * q + 2], v.z * ap.decay);
-      v.w = fmaf(-lrs, o[4 * q + 3], v.w * ap.decay);
+      v.x = fmaf(-lrs, o[4 * q + 0], v.x * decay);
+      v.y = fmaf(-lrs, o[4 * q + 1], v.y * decay);
+      v.z = fmaf(-lrs, o[4 * q + 2], v.z * decay);
+      v.w = fmaf(-lrs, o[4 * q + 3], v.w * decay);
       w[q] = v;
     }
   } else {
@@ -285,7 +293,7 @@ __device__ __forceinline__ void apply_row_run(const ApplyArgs& ap, const MatDev&
         const long long g = g0 + t;
         const long long s = g / ap.L;
         float* w = ap.W.p[s] + (g - s * ap.L);
-        *w = fmaf(-lrs, o[t], *w * ap.decay);
+        *w = fmaf(-lrs, o[t], *w * decay);
       }
     }
   }
@@ -317,17 +325,18 @@ __device__ __forceinline__ void apply_store_row_run(const ApplyArgs& ap, const M
     apply_row_run(ap, mt, i, jb, 32, o);
     return;
   }
-  const float lrs = ap.lr * mt.scale;
+  const float lrs = ap.gp.lr[mt.group] * mt.scale;
+  const float decay = ap.gp.decay[mt.group];
   const long long g0 = mt.flat_off + (long long)i * mt.cols + jb;
   const long long s0 = g0 / ap.L;
   float4* dst = reinterpret_cast<float4*>(ap.W.p[s0] + (g0 - s0 * ap.L));
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     float4 v;
-    v.x = fmaf(-lrs, o[4 * q + 0], w[4 * q + 0] * ap.decay);
-    v.y = fmaf(-lrs, o[4 * q + 1], w[4 * q + 1] * ap.decay);
-    v.z = fmaf(-lrs, o[4 * q + 2], w[4 * q + 2] * ap.decay);
-    v.w = fmaf(-lrs, o[4 * q + 3], w[4 * q + 3] * ap.decay);
+    v.x = fmaf(-lrs, o[4 * q + 0], w[4 * q + 0] * decay);
+    v.y = fmaf(-lrs, o[4 * q + 1], w[4 * q + 1] * decay);
+    v.z = fmaf(-lrs, o[4 * q + 2], w[4 * q + 2] * decay);
+    v.w = fmaf(-lrs, o[4 * q + 3], w[4 * q + 3] * decay);
     dst[q] = v;
   }
 }

@@ -12,6 +12,7 @@ namespace muon {
 
 struct ShardPtrs;
 struct ApplyArgs;
+struct GroupParams;
 
 // Device-resident tables of a layout (uploaded once per device).
 struct DevTables {
@@ -31,7 +32,7 @@ struct DevTables {
 
 // Stage 1: momentum, orthogonalization input into X0, per-chunk sums of squares.
 cudaError_t launch_momentum_input(const Plan& plan, const DevTables& dt, const ShardPtrs& g,
-                                  const ShardPtrs& m, void* ws, float mu, int nesterov,
+                                  const ShardPtrs& m, void* ws, const GroupParams& gp,
                                   cudaStream_t st);
 // Full fp32 matrices -> X0 plus per-chunk sums of squares.
 cudaError_t launch_full_input(const Plan& plan, const DevTables& dt, const float* full, void* ws,
@@ -41,8 +42,8 @@ cudaError_t launch_norm_finalize(const Plan& plan, const DevTables& dt, void* ws
                                  cudaStream_t st);
 // Stage 3: W <- W*decay - lr*scale*O, O read from the final X buffer.
 cudaError_t launch_apply(const Plan& plan, const DevTables& dt, const ShardPtrs& w,
-                         const void* ws, int final_buf, int pending_norm, float decay,
-                         float lr, cudaStream_t st);
+                         const void* ws, int final_buf, int pending_norm, const GroupParams& gp,
+                         cudaStream_t st);
 // Owner gather / scatter between shards and the fp32 full layout.
 cudaError_t launch_gather(const Plan& plan, const DevTables& dt, const ShardPtrs& src,
                           float* full, cudaStream_t st);

@@ -92,6 +92,7 @@ std::string build_plan(const int64_t* shapes, const uint8_t* is_matrix, int32_t 
     m.full_off = p.full_off[i];
     m.flat_off = p.flat_off[i];
     m.scale = (float)std::sqrt(std::max(1.0, (double)m.rows / (double)m.cols));
+    m.group = 0;
     m.chunk_begin = (int64_t)p.chunks.size();
     const int64_t numel = (int64_t)m.rows * m.cols;
     const bool dense_x = (m.ldx == m.cols);

@@ -18,6 +18,9 @@ constexpr int kChunkElems = 32768;
 // Workspace alignment of every per-matrix buffer (TMA wants 16 B; SW128 tiles 1024 B).
 constexpr int64_t kWsAlign = 1024;
 
+// Optimizer groups whose hyper-parameters a call can carry (by value, in kernel arguments).
+constexpr int kMaxGroups = 32;
+
 // tcgen05 NS tile (bf16 path) and SIMT NS tile (fp32 path).
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 256;
@@ -57,7 +60,7 @@ struct MatDev {            // 104 bytes
   int64_t chunk_begin;     // chunk table range of this matrix
   int64_t chunk_end;
   float scale;             // sqrt(max(1, rows/cols))
-  float pad_;
+  int32_t group;           // optimizer group (index into per-call hyper-parameters)
   int64_t flat_off;        // element offset of the matrix in the unsharded flat buffer
 };
 
@@ -86,6 +89,7 @@ struct Plan {
   std::vector<uint8_t> is_matrix;
   std::vector<int64_t> flat_off;      // per parameter
   std::vector<int64_t> full_off;      // per parameter, -1 for non-matrix
+  int32_t n_groups = 1;               // optimizer groups (muon_layout_set_groups)
   std::vector<MatDev> mats;           // matrix parameters with numel > 0
   std::vector<ChunkDev> chunks;
   // Workspace: [partials: n_chunks f32][inv_norm: n_mats f32][per-matrix buffers]

@@ -94,12 +94,14 @@ template <typename XT>
 __global__ void __launch_bounds__(kThreads)
 momentum_input_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
                       const MatDev* __restrict__ mats, ShardPtrs G, ShardPtrs M, int64_t L,
-                      uint8_t* __restrict__ ws, float* __restrict__ partials, float mu,
-                      int nesterov) {
+                      uint8_t* __restrict__ ws, float* __restrict__ partials,
+                      const __grid_constant__ GroupParams gp) {
   __shared__ float red[32];
   for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
     const ChunkDev ch = chunks[ci];
     const MatDev& mt = mats[ch.mat];
+    const float mu = gp.mu[mt.group];
+    const int nesterov = gp.nesterov[mt.group];
     XT* __restrict__ x = reinterpret_cast<XT*>(ws + mt.x0);
     const int nv = ch.len >> 2;
     float ss = 0.f;
@@ -243,12 +245,13 @@ __global__ void __launch_bounds__(kThreads)
 apply_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
              const MatDev* __restrict__ mats, ShardPtrs W, int64_t L,
              const uint8_t* __restrict__ ws,
-             int final_buf, const float* __restrict__ inv_norm, int pending_norm, float decay,
-             float lr) {
+             int final_buf, const float* __restrict__ inv_norm, int pending_norm,
+             const __grid_constant__ GroupParams gp) {
   for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
     const ChunkDev ch = chunks[ci];
     const MatDev& mt = mats[ch.mat];
-    float lrs = lr * mt.scale;
+    float lrs = gp.lr[mt.group] * mt.scale;
+    const float decay = gp.decay[mt.group];
     if (pending_norm) lrs *= inv_norm[ch.mat];
     const XT* __restrict__ o = reinterpret_cast<const XT*>(ws + (final_buf ? mt.x1 : mt.x0));
     if (ch.vec) {
@@ -357,7 +360,7 @@ int grid_for(const Plan& plan, const DevTables& dt) {
 }  // namespace
 
 cudaError_t launch_momentum_input(const Plan& plan, const DevTables& dt, const ShardPtrs& g,
-                                  const ShardPtrs& m, void* ws, float mu, int nesterov,
+                                  const ShardPtrs& m, void* ws, const GroupParams& gp,
                                   cudaStream_t st) {
   const int grid = grid_for(plan, dt);
   if (grid == 0) return cudaSuccess;
@@ -365,10 +368,10 @@ cudaError_t launch_momentum_input(const Plan& plan, const DevTables& dt, const S
   float* partials = reinterpret_cast<float*>(w + plan.ws_partials);
   if (plan.ns_dtype == 0)
     momentum_input_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
-        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, plan.L, w, partials, mu, nesterov);
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, plan.L, w, partials, gp);
   else
     momentum_input_kernel<float><<<grid, kThreads, 0, st>>>(
-        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, plan.L, w, partials, mu, nesterov);
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, plan.L, w, partials, gp);
   return cudaGetLastError();
 }
 
@@ -400,8 +403,8 @@ cudaError_t launch_norm_finalize(const Plan& plan, const DevTables& dt, void* ws
 }
 
 cudaError_t launch_apply(const Plan& plan, const DevTables& dt, const ShardPtrs& wp,
-                         const void* ws, int final_buf, int pending_norm, float decay,
-                         float lr, cudaStream_t st) {
+                         const void* ws, int final_buf, int pending_norm, const GroupParams& gp,
+                         cudaStream_t st) {
   const int grid = grid_for(plan, dt);
   if (grid == 0) return cudaSuccess;
   const uint8_t* w = static_cast<const uint8_t*>(ws);
@@ -409,11 +412,11 @@ cudaError_t launch_apply(const Plan& plan, const DevTables& dt, const ShardPtrs&
   if (plan.ns_dtype == 0)
     apply_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
         dt.chunks, (int64_t)plan.chunks.size(), dt.mats, wp, plan.L, w, final_buf, inv,
-        pending_norm, decay, lr);
+        pending_norm, gp);
   else
     apply_kernel<float><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
                                                    dt.mats, wp, plan.L, w, final_buf, inv,
-                                                   pending_norm, decay, lr);
+                                                   pending_norm, gp);
   return cudaGetLastError();
 }
 

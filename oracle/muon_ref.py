@@ -262,3 +262,26 @@ def muon_step_sharded(W_shards, G_shards, M_shards, layout, lr, wd, mu, nesterov
         loc = owned[s * L: (s + 1) * L]
         W_sh[s][loc] = W_sh[s][loc] - U_sh[s][loc]
     return W_sh, M_sh, updates
+
+
+def muon_step_grouped(W, G, M, layout, group_of, hparams, ns_steps=5):
+    """One step with per-group hyper-parameters (Megatron-Core API page, class
+    _FsdpGroupAssignment: tensor_to_optimizer_group_index maps each tensor to the
+    optimizer group whose settings it uses).  ``group_of[i]`` is parameter i's group;
+    ``hparams[g]`` = (lr, wd, mu, nesterov).  Returns (W_new, M_new, updates)."""
+    W = np.array(W, dtype=np.float64, copy=True)
+    M = np.array(M, dtype=np.float64, copy=True)
+    G = np.asarray(G, dtype=np.float64)
+    updates = {}
+    for i, (r, c) in enumerate(layout["shapes"]):
+        if not layout["is_matrix"][i]:
+            continue
+        lr, wd, mu, nesterov = hparams[group_of[i]]
+        sl = slice(layout["offsets"][i], layout["offsets"][i] + r * c)
+        Wd = weight_decay(W[sl], lr, wd)
+        M[sl] = momentum_update(M[sl], G[sl], mu)
+        X = ns_input(G[sl], M[sl], mu, nesterov).reshape(r, c)
+        O = newton_schulz(X, ns_steps)
+        updates[i] = O
+        W[sl] = apply_update(Wd, O.reshape(-1), lr, r, c)
+    return W, M, updates

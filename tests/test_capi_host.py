@@ -113,3 +113,14 @@ def test_step_validates_before_any_launch():
                             None)
     assert st == capi.MUON_ERR_INVALID_ARG
     assert capi.lib.muon_selftest_wait_timeout(0, None) == capi.MUON_ERR_INVALID_ARG
+
+
+def test_set_groups_validation_on_host():
+    lay = capi.muon_layout_create([(4, 4), (3, 1)], 1, 0, [True, False])
+    with pytest.raises(capi.MuonError):
+        capi.muon_layout_set_groups(lay, [2, 0], 2)
+    capi.muon_layout_set_groups(lay, [1, 99], 2)  # non-matrix entry is ignored
+    with pytest.raises(capi.MuonError):
+        capi.muon_layout_set_groups(lay, [0, 0], 33)
+    with pytest.raises(capi.MuonError):
+        capi.muon_layout_set_groups(lay, [0, 0], 0)

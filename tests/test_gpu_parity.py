@@ -362,3 +362,65 @@ def test_each_tcgen05_variant_vs_oracle(capi, variant, monkeypatch):
     for i, Xi in X.items():
         e = rel(got[i], ref.newton_schulz(Xi.astype(np.float32).astype(np.float64), 5))
         assert e < TOL_NS[0], (variant, wl.shapes[i], e)
+
+
+GROUP_HP = [(0.02, 0.01, 0.95, True), (0.05, 0.0, 0.9, False), (0.001, 0.1, 0.5, True)]
+
+
+def test_grouped_step_fp32_vs_oracle(capi):
+    """Per-group lr / wd / mu / Nesterov on the fp32 path, stage by stage against the
+    oracle's grouped step (momentum and weights 1e-6, update 1e-4)."""
+    wl = inputs.WORKLOADS["ragged_small"]
+    W0, Gs, M0 = inputs.host_inputs(wl)
+    M0 = (np.random.default_rng(1).normal(0, 1e-3, M0.size)).astype(np.float32)
+    group_of = [i % 3 for i in range(len(wl.shapes))]
+    lay = capi.muon_layout_create(wl.shapes, 3, 1, wl.is_matrix)
+    capi.muon_layout_set_groups(lay, group_of, 3)
+    ws = capi.workspace_tensor(lay)
+    W, M, G = split_shards(W0, 3), split_shards(M0, 3), split_shards(Gs[0], 3)
+    capi.muon_step_grouped(W, G, M, lay, ws, GROUP_HP, 5)
+    O = torch.zeros(lay.full_numel, device="cuda")
+    capi.muon_export_update(lay, ws, 5, O)
+    capi.muon_check()
+    o = ref.flat_layout(wl.shapes, 1, wl.is_matrix)
+    W_or, M_or, upd = ref.muon_step_grouped(W0, Gs[0], M0, o, group_of, GROUP_HP, 5)
+    Wg, Mg = join_shards(W, lay.numel), join_shards(M, lay.numel)
+    Og = full_to_mats(O, lay, wl)
+    for i, (r, c) in enumerate(wl.shapes):
+        sl = slice(o["offsets"][i], o["offsets"][i] + r * c)
+        if not wl.is_matrix[i]:
+            assert np.array_equal(Wg[sl], W0[sl]) and np.array_equal(Mg[sl], M0[sl])
+            continue
+        lr, wd, mu, nest = GROUP_HP[group_of[i]]
+        assert rel(Mg[sl], M_or[sl]) < TOL_STATE, i
+        assert rel(Og[i], upd[i]) < TOL_NS[1], i
+        want = ref.apply_update(ref.weight_decay(W0[sl], lr, wd), Og[i].reshape(-1), lr, r, c)
+        assert rel(Wg[sl], want) < TOL_STATE, i
+
+
+def test_grouped_step_bf16_equals_ungrouped_per_group(capi):
+    """On the tensor-core path each matrix's result depends only on its own group's
+    values: the grouped step equals, bit for bit, the plain step run with that group's
+    scalars (same layout, so the same kernels and tiles)."""
+    wl = inputs.WORKLOADS["ragged_small"]
+    W0, Gs, M0 = inputs.host_inputs(wl)
+    group_of = [i % 3 for i in range(len(wl.shapes))]
+    lay = capi.muon_layout_create(wl.shapes, 2, 0, wl.is_matrix)
+    capi.muon_layout_set_groups(lay, group_of, 3)
+    ws = capi.workspace_tensor(lay)
+    W, M, G = split_shards(W0, 2), split_shards(M0, 2), split_shards(Gs[0], 2)
+    capi.muon_step_grouped(W, G, M, lay, ws, GROUP_HP, 5)
+    capi.muon_check()
+    Wg, Mg = join_shards(W, lay.numel), join_shards(M, lay.numel)
+    o = ref.flat_layout(wl.shapes, 1, wl.is_matrix)
+    for g, (lr, wd, mu, nest) in enumerate(GROUP_HP):
+        W1, M1, G1 = split_shards(W0, 2), split_shards(M0, 2), split_shards(Gs[0], 2)
+        capi.muon_step(W1, G1, M1, lay, ws, lr, wd, mu, nest, 5)
+        capi.muon_check()
+        Wu, Mu = join_shards(W1, lay.numel), join_shards(M1, lay.numel)
+        for i, (r, c) in enumerate(wl.shapes):
+            if wl.is_matrix[i] and group_of[i] == g:
+                sl = slice(o["offsets"][i], o["offsets"][i] + r * c)
+                assert np.array_equal(Wg[sl], Wu[sl]), (g, i)
+                assert np.array_equal(Mg[sl], Mu[sl]), (g, i)
+

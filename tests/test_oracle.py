@@ -362,3 +362,29 @@ def test_input_generators_are_seeded_and_shaped():
     assert inputs.WORKLOADS["gpt2_small_x12"].numel == 84_934_656
     assert inputs.WORKLOADS["moe_64e"].numel == 570_425_344
     assert inputs.WORKLOADS["moe_64e"].n_matrices == 196
+
+
+def test_grouped_step_matches_per_group_steps_and_closed_form():
+    wl = inputs.WORKLOADS["ragged_small"]
+    W0, Gs, M0 = inputs.host_inputs(wl)
+    M0 = np.random.default_rng(1).normal(0, 1e-3, M0.size)
+    lay = ref.flat_layout(wl.shapes, 1, wl.is_matrix)
+    group_of = [i % 3 for i in range(len(wl.shapes))]
+    hp = [(0.02, 0.01, 0.95, True), (0.05, 0.0, 0.9, False), (0.001, 0.1, 0.5, True)]
+    W, M, upd = ref.muon_step_grouped(W0, Gs[0], M0, lay, group_of, hp, 5)
+    for g, (lr, wd, mu, nest) in enumerate(hp):
+        Wg, Mg, ug = ref.muon_step(W0, Gs[0], M0, lay, lr, wd, mu, nest, 5)
+        for i, (r, c) in enumerate(wl.shapes):
+            if not wl.is_matrix[i] or group_of[i] != g:
+                continue
+            sl = slice(lay["offsets"][i], lay["offsets"][i] + r * c)
+            np.testing.assert_array_equal(W[sl], Wg[sl])
+            np.testing.assert_array_equal(M[sl], Mg[sl])
+    # group 1 has no Nesterov: X = M1 = 0.9 M0 + G, W1 = W0 (1 - 0) - 0.05 s NS(X)
+    i = 4  # (1, 50): group 1
+    assert group_of[i] == 1
+    r, c = wl.shapes[i]
+    sl = slice(lay["offsets"][i], lay["offsets"][i] + r * c)
+    X = (0.9 * M0[sl] + Gs[0][sl].astype(np.float64)).reshape(r, c)
+    want = W0[sl].astype(np.float64) - 0.05 * 1.0 * ref.newton_schulz(X).reshape(-1)
+    assert rel(W[sl], want) < 1e-15
