@@ -278,6 +278,17 @@ def _pin_to_gpu_numa_node(dev):
         pass
 
 
+def reduce_max_over_ranks(values, dist, device):
+    """Element-wise max of a list of floats over all ranks (the timing rule: the slowest
+    rank sets the step time); identity without a process group."""
+    if dist is None:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
 def run_ours(args):
     import torch
     from muon_optimizer_step_gb300 import capi, inputs
@@ -353,10 +364,8 @@ def run_ours(args):
         for j in range(2):
             stage_ms[j] += e[j].elapsed_time(e[j + 1])
     stage_ms = [x / args.steps for x in stage_ms]
-    if dist is not None:
-        t = torch.tensor([total_ms] + stage_ms, device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, stage_ms = float(t[0]), [float(x) for x in t[1:]]
+    red = reduce_max_over_ranks([total_ms] + stage_ms, dist, dev)
+    total_ms, stage_ms = red[0], red[1:]
     ms = total_ms / args.steps
 
     # ------------------------------------------------------------ end to end (host buffers)
@@ -418,10 +427,7 @@ def run_ours(args):
             b.record(comp)
             torch.cuda.synchronize()
             e2e_ms = a.elapsed_time(b) / n_e2e
-            if dist is not None:
-                t_ = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-                dist.all_reduce(t_, op=dist.ReduceOp.MAX)
-                e2e_ms = float(t_[0])
+            e2e_ms = reduce_max_over_ranks([e2e_ms], dist, dev)[0]
             e2e = {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": 4 * N,
                    "d2h_bytes_per_step": 4 * N, "steps": n_e2e,
                    "note": "per step: gradient H2D from pinned host memory, the three stage "

@@ -166,6 +166,19 @@ muon_status muon_orthogonalize_apply(float* const* flat_params, const muon_layou
                                      void* workspace, float lr, float wd, int32_t ns_steps,
                                      cudaStream_t stream);
 
+/* ---------------------------------------------------------------- owner assignment
+ * [P1] "What does this PR do?": for each sharded matrix one owner that holds at least one
+ * of its shards is picked, and "Opt step" step 3: the owner is picked heuristically
+ * depending on orthogonalization compute cost ([P2] tensor_to_owner_rank, computed once).
+ * muon_assign_owners plans this for a data-parallel group of n_shards ranks (rank r holds
+ * shard r): matrices in decreasing Newton-Schulz cost 5*(3 m^2 n + m^3)*ns_steps/5, each to
+ * the least-loaded rank among those holding a part of it (ties: lowest rank), so a matrix
+ * inside one shard stays on its rank ("computed fully locally").  owner: host array of
+ * n_params entries (-1 for non-matrix parameters); rank_cost: host array of n_shards flop
+ * totals, or NULL.  Pure host work, deterministic, so every rank computes the same plan. */
+muon_status muon_assign_owners(const muon_layout* layout, int32_t ns_steps, int32_t* owner,
+                               double* rank_cost);
+
 /* ---------------------------------------------------------------- owner gather / scatter
  * [P1] "Opt step" step 3 (gather on the owner) and step 5 (scatter from the owner) as
  * pure index maps between the shards and the fp32 full layout.  Bit copies.

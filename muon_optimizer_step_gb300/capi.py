@@ -60,6 +60,7 @@ SIGNATURES = [
     ("muon_orthogonalize_apply", _I32, [_PP, _P, _P, _F, _F, _I32, _P]),
     ("muon_layout_set_groups", _I32, [_P, ctypes.POINTER(_I32), _I32]),
     ("muon_step_grouped", _I32, [_PP, _PP, _PP, _P, _P, ctypes.POINTER(GroupHparams), _I32, _P]),
+    ("muon_assign_owners", _I32, [_P, _I32, ctypes.POINTER(_I32), ctypes.POINTER(ctypes.c_double)]),
     ("muon_gather_full", _I32, [_P, _PP, _P, _P]),
     ("muon_scatter_updates", _I32, [_P, _P, _PP, _P]),
     ("muon_orthogonalize_full", _I32, [_P, _P, _P, _P, _I32, _P]),
@@ -259,6 +260,14 @@ def muon_orthogonalize_apply(flat_params, layout, workspace, lr, wd, ns_steps=5,
                                         layout.handle, _ptr(workspace), float(lr), float(wd),
                                         int(ns_steps), _stream_handle(stream)),
            "muon_orthogonalize_apply")
+
+
+def muon_assign_owners(layout, ns_steps=5):
+    """(owner per parameter, flop total per rank) for one rank per shard."""
+    owner = (_I32 * max(1, len(layout.shapes)))()
+    cost = (ctypes.c_double * max(1, layout.n_shards))()
+    _check(lib.muon_assign_owners(layout.handle, int(ns_steps), owner, cost), "muon_assign_owners")
+    return [owner[i] for i in range(len(layout.shapes))], [cost[s] for s in range(layout.n_shards)]
 
 
 def muon_gather_full(layout, shards, full, stream=None):

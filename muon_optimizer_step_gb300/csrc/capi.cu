@@ -489,6 +489,15 @@ muon_status muon_layout_set_groups(muon_layout* layout, const int32_t* group_of,
   return ok();
 }
 
+muon_status muon_assign_owners(const muon_layout* layout, int32_t ns_steps, int32_t* owner,
+                               double* rank_cost) {
+  if (layout == nullptr) return fail(MUON_ERR_INVALID_ARG, "layout is NULL");
+  if (owner == nullptr && layout->plan.n_params > 0) return fail(MUON_ERR_INVALID_ARG, "owner is NULL");
+  MUON_TRY(check_steps(ns_steps));
+  assign_owners(layout->plan, ns_steps, owner, rank_cost);
+  return ok();
+}
+
 muon_status muon_step_grouped(float* const* flat_params, const float* const* flat_grads,
                               float* const* flat_momentum, const muon_layout* layout,
                               void* workspace, const muon_group_hparams* groups, int32_t ns_steps,

@@ -207,6 +207,38 @@ TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_s
   return tl;
 }
 
+void assign_owners(const Plan& plan, int ns_steps, int32_t* owner, double* rank_cost) {
+  const int S = plan.n_shards;
+  std::vector<double> load(S, 0.0);
+  struct Job { double cost; int32_t param; int64_t first, last; };
+  std::vector<Job> jobs;
+  for (int32_t i = 0; i < plan.n_params; ++i) {
+    owner[i] = -1;
+    if (!plan.is_matrix[i]) continue;
+    const double r = (double)plan.rows[i], c = (double)plan.cols[i];
+    const double m = std::min(r, c), n = std::max(r, c);
+    Job j;
+    j.cost = (double)ns_steps * (3.0 * m * m * n + m * m * m);
+    j.param = i;
+    const int64_t numel = plan.rows[i] * plan.cols[i];
+    j.first = plan.flat_off[i] / plan.L;
+    j.last = (plan.flat_off[i] + numel - 1) / plan.L;
+    jobs.push_back(j);
+  }
+  // Most expensive first; equal costs keep the parameters' order.
+  std::stable_sort(jobs.begin(), jobs.end(),
+                   [](const Job& a, const Job& b) { return a.cost > b.cost; });
+  for (const Job& j : jobs) {
+    int64_t best = j.first;
+    for (int64_t s = j.first + 1; s <= j.last; ++s)
+      if (load[s] < load[best]) best = s;
+    owner[j.param] = (int32_t)best;
+    load[best] += j.cost;
+  }
+  if (rank_cost != nullptr)
+    for (int s = 0; s < S; ++s) rank_cost[s] = load[s];
+}
+
 int64_t tile_makespan(const TileList& tl, int phase, int per_tile_units) {
   int64_t worst = 0;
   const int64_t epi = phase == kPhaseUpdate ? 2 : 3;

@@ -105,6 +105,12 @@ std::string build_plan(const int64_t* shapes, const uint8_t* is_matrix, int32_t 
 // Longest-processing-time assignment of a phase's tiles to `grid` CTAs (grid <= n_sms).
 TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_sms);
 
+// Owner of every matrix parameter for an n_shards-rank data-parallel group (one shard per
+// rank): longest Newton-Schulz cost first, each to the least-loaded rank among those that
+// hold a shard of it (ties: lowest rank).  owner[i] = -1 for non-matrix parameters;
+// rank_cost[r] receives each rank's total cost in flops for ns_steps iterations.
+void assign_owners(const Plan& plan, int ns_steps, int32_t* owner, double* rank_cost);
+
 // Largest per-CTA load of a tile list, in the cost units plan_tiles balances
 // (k-blocks of 128 x 256 x 64 MMA work plus an epilogue allowance per tile).
 int64_t tile_makespan(const TileList& tl, int phase, int per_tile_units);

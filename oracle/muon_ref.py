@@ -285,3 +285,42 @@ def muon_step_grouped(W, G, M, layout, group_of, hparams, ns_steps=5):
         updates[i] = O
         W[sl] = apply_update(Wd, O.reshape(-1), lr, r, c)
     return W, M, updates
+
+
+# --------------------------------------------------------------------------------------
+# Owner choice ("Add initial Muon+M-FSDPv2 implementation", "What does this PR do?": one
+# owner holding at least one shard of the matrix; "Opt step" step 3: picked by
+# orthogonalization compute cost).  The pages give no rule beyond that; this oracle
+# reads it as longest-processing-time first onto the least-loaded eligible rank.
+# --------------------------------------------------------------------------------------
+def ns_cost(rows, cols, ns_steps=5):
+    """Newton-Schulz flops of one matrix with symmetric Gram and A^2 (per the iteration:
+    m^2 n + m^3 + 2 m^2 n per step, m = min, n = max of the shape)."""
+    m, n = min(rows, cols), max(rows, cols)
+    return ns_steps * (m * m * n + m ** 3 + 2 * m * m * n)
+
+
+def shards_of(layout, i):
+    """The shard indices holding a part of parameter i."""
+    r, c = layout["shapes"][i]
+    L = layout["L"]
+    first = layout["offsets"][i] // L
+    last = (layout["offsets"][i] + r * c - 1) // L
+    return list(range(first, last + 1))
+
+
+def assign_owners(layout, ns_steps=5):
+    """(owner per parameter, cost per rank): each matrix, most expensive first (ties in
+    parameter order), to the least-loaded rank among its shards (ties: lowest rank)."""
+    S = layout["n_shards"]
+    load = [0.0] * S
+    owner = [-1] * len(layout["shapes"])
+    jobs = [(ns_cost(r, c, ns_steps), i) for i, (r, c) in enumerate(layout["shapes"])
+            if layout["is_matrix"][i]]
+    jobs.sort(key=lambda t: (-t[0], t[1]))
+    for cost, i in jobs:
+        cands = shards_of(layout, i)
+        best = min(cands, key=lambda s: (load[s], s))
+        owner[i] = best
+        load[best] += cost
+    return owner, load
