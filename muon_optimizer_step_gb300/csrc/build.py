@@ -20,8 +20,8 @@ ROOT = os.path.dirname(PKG)
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libmuon.so")
 
-SOURCES = ["layout.cpp", "capi.cu", "stream_kernels.cu", "gemm_f32.cu", "gemm_tc.cu",
-           "gemm_tc2.cu", "noalloc.cu"]
+SOURCES = ["layout.cpp", "capi.cu", "stream_kernels.cu", "gemm_f32.cu", "gemm_ns.cu",
+           "noalloc.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -7,6 +7,7 @@
 // index maps fused into the first and last kernels.
 #include <cmath>
 #include <cstdarg>
+#include <algorithm>
 #include <cstdlib>
 #include <cstdio>
 #include <cstring>
@@ -118,52 +119,57 @@ muon_status ensure_device(muon_layout* L) {
   muon_status s;
   if ((s = err_word(dev, &t.err)) != MUON_OK) return s;
   if ((s = upload(L->plan.chunks, &t.chunks)) != MUON_OK) { free_tables(&t); return s; }
-  if ((s = upload(L->plan.mats, &t.mats)) != MUON_OK) { free_tables(&t); return s; }
   const bool bf16 = L->plan.ns_dtype == MUON_NS_BF16;
-  int pairs = sms / 2;
-  int forced = 0;  // MUON_TC_KERNEL=1 or 2 pins one tcgen05 variant (for measurements)
-  if (bf16) {
-    const char* v = std::getenv("MUON_TC_KERNEL");
-    if (v != nullptr && (v[0] == '1' || v[0] == '2')) forced = v[0] - '0';
-    e = prepare_tc2_kernel(&pairs);
-    if (e != cudaSuccess) { free_tables(&t); return cuda_fail(e, "prepare pair kernel"); }
-    if (pairs > sms / 2) pairs = sms / 2;
-  }
-  for (int p = 0; p < 3; ++p) {
-    TileList tl;
-    if (!bf16) {
-      tl = plan_tiles(L->plan, p, kF32BM, kF32BN, 16, sms);
-    } else {
-      // Per phase: CTA pairs (256 x 256 tiles, a third less operand traffic per k-block)
-      // when most of the phase's MMA work sits in matrices that span at least ten 256-wide
-      // tiles; single CTAs (128 x 256 tiles) otherwise, where the finer tiles balance
-      // better.  Measured on GB300: pairs are 4-7% faster on the Llama-3-8B set and 7-10%
-      // slower on the GPT-2 and MoE sets.
-      TileList t1 = plan_tiles(L->plan, p, kTcBM, kTcBN, kTcBK, sms);
-      double big = 0.0, all = 0.0;
-      for (const TileDev& td : t1.tiles) {
-        all += td.kblocks;
-        if (L->plan.mats[td.mat].m >= 2560) big += td.kblocks;
-      }
-      int variant = (pairs >= 1 && big >= 0.5 * all) ? 2 : 1;
-      if (forced != 0) variant = forced;
-      if (variant == 2 && pairs < 1) {
-        free_tables(&t);
-        return fail(MUON_ERR_UNSUPPORTED, "no CTA pair fits on the device");
-      }
-      t.tc_variant[p] = variant;
-      tl = variant == 2 ? plan_tiles(L->plan, p, 256, 256, kTcBK, pairs) : std::move(t1);
+  if (!bf16) {
+    for (int p = 0; p < 3; ++p) {
+      const TileList tl = plan_tiles(L->plan, p, kF32BM, kF32BN, 16, sms);
+      t.grid[p] = tl.grid;
+      if ((s = upload(tl.tiles, &t.tiles[p])) != MUON_OK) { free_tables(&t); return s; }
+      if ((s = upload(tl.cta_begin, &t.cta_begin[p])) != MUON_OK) { free_tables(&t); return s; }
     }
-    t.grid[p] = tl.grid;
-    if ((s = upload(tl.tiles, &t.tiles[p])) != MUON_OK) { free_tables(&t); return s; }
-    if ((s = upload(tl.cta_begin, &t.cta_begin[p])) != MUON_OK) { free_tables(&t); return s; }
-  }
-  if (bf16 && !L->plan.mats.empty()) {
+  } else if (!L->plan.mats.empty()) {
+    int pairs = 0;
+    e = prepare_ns_kernels(&pairs);
+    if (e != cudaSuccess) { free_tables(&t); return cuda_fail(e, "prepare tcgen05 kernels"); }
+    pairs = std::min(pairs, sms / 2);
+    // CTA pairs (256 x 256 tiles, a third less operand traffic per k-block) when most of
+    // the MMA work sits in matrices that span at least ten 256-wide tiles; single CTAs
+    // (128 x 256 tiles) otherwise, where the finer tiles balance better.  Measured on
+    // GB300: pairs 4-7% faster on the Llama-3-8B set, 7-10% slower on GPT-2 and MoE.
+    double big = 0.0, all = 0.0;
+    for (const MatDev& m : L->plan.mats) {
+      const double work = 3.0 * m.m * (double)m.m * m.n + (double)m.m * m.m * m.m;
+      all += work;
+      if (m.m >= 2560) big += work;
+    }
+    bool pair = pairs >= 1 && big >= 0.5 * all;
+    const char* v = std::getenv("MUON_TC_KERNEL");  // "1" / "2" pins a shape (measurements)
+    if (v != nullptr && v[0] == '1') pair = false;
+    if (v != nullptr && v[0] == '2' && pairs >= 1) pair = true;
+    t.tc_pair = pair;
+    t.tc_units = pair ? pairs : sms;
+    // One persistent launch when a phase carries little work (< 100 GFLOP, e.g. the
+    // GPT-2-small set: 8% faster there); a launch per phase otherwise (Llama-3-8B: twice as
+    // fast as persistent; MoE: 16% faster), where each phase's tiles are balanced alone.
+    t.tc_persistent = all / 3.0 < 100e9;
+    const char* pv = std::getenv("MUON_NS_PERSISTENT");  // "1" / "0" pins the launch mode
+    if (pv != nullptr && (pv[0] == '0' || pv[0] == '1')) t.tc_persistent = pv[0] == '1';
+    for (MatDev& m : L->plan.mats) m.sig[0] = m.sig[1] = m.sig[2] = 0;
+    for (int p = 0; p < 3; ++p) {
+      TileList tl = pair ? plan_tiles(L->plan, p, 256, 256, kTcBK, t.tc_units, !t.tc_persistent)
+                         : plan_tiles(L->plan, p, kTcBM, kTcBN, kTcBK, t.tc_units,
+                                      !t.tc_persistent);
+      // Every unit of the persistent launch reads begin[unit + 1]: pad the offsets.
+      while ((int)tl.cta_begin.size() < t.tc_units + 1) tl.cta_begin.push_back(tl.cta_begin.back());
+      for (const TileDev& td : tl.tiles) L->plan.mats[td.mat].sig[p] += pair ? 2 : 1;
+      t.grid[p] = tl.grid;
+      if ((s = upload(tl.tiles, &t.tiles[p])) != MUON_OK) { free_tables(&t); return s; }
+      if ((s = upload(tl.cta_begin, &t.cta_begin[p])) != MUON_OK) { free_tables(&t); return s; }
+    }
     e = cudaMalloc(&t.tmaps, L->plan.mats.size() * kMapsPerMat * sizeof(CUtensorMap));
     if (e != cudaSuccess) { free_tables(&t); return fail(MUON_ERR_OOM, "cudaMalloc(tensor maps)"); }
-    e = prepare_tc_kernel();
-    if (e != cudaSuccess) { free_tables(&t); return cuda_fail(e, "cudaFuncSetAttribute"); }
   }
+  if ((s = upload(L->plan.mats, &t.mats)) != MUON_OK) { free_tables(&t); return s; }
   dt = t;
   return MUON_OK;
 }
@@ -256,21 +262,14 @@ muon_status run_momentum(muon_layout* L, const ShardPtrs& g, const ShardPtrs& m,
 }
 
 muon_status run_ns(muon_layout* L, void* ws, int ns_steps, const ApplyArgs* ap, cudaStream_t st) {
-  for (int it = 0; it < ns_steps; ++it) {
-    const int x_in = it & 1;
-    const int iter0 = it == 0 ? 1 : 0;
-    for (int ph = 0; ph < 3; ++ph) {
-      const ApplyArgs* fuse = (ph == kPhaseUpdate && it == ns_steps - 1) ? ap : nullptr;
-      cudaError_t e;
-      if (L->plan.ns_dtype != MUON_NS_BF16)
-        e = launch_ns_phase_f32(L->plan, L->dt, ws, ph, x_in, iter0, st);
-      else if (L->dt.tc_variant[ph] == 2)
-        e = launch_ns_phase_tc2(L->plan, L->dt, ws, ph, x_in, iter0, kDefaultBudget, fuse, st);
-      else
-        e = launch_ns_phase_tc(L->plan, L->dt, ws, ph, x_in, iter0, kDefaultBudget, fuse, st);
-      if (e != cudaSuccess) return cuda_fail(e, "newton_schulz phase");
-    }
+  if (L->plan.ns_dtype == MUON_NS_BF16) {
+    MUON_CUDA(launch_ns_tc(L->plan, L->dt, ws, ns_steps, kDefaultBudget, ap, st), "newton_schulz");
+    return MUON_OK;
   }
+  for (int it = 0; it < ns_steps; ++it)
+    for (int ph = 0; ph < 3; ++ph)
+      MUON_CUDA(launch_ns_phase_f32(L->plan, L->dt, ws, ph, it & 1, it == 0 ? 1 : 0, st),
+                "newton_schulz phase");
   return MUON_OK;
 }
 

@@ -279,12 +279,12 @@ __device__ __forceinline__ void apply_row_run(const ApplyArgs& ap, const MatDev&
     float4* w = reinterpret_cast<float4*>(ap.W.p[s0] + off0);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      float4 v = w[q];
+      float4 v = __ldcs(w + q);
       v.x = fmaf(-lrs, o[4 * q + 0], v.x * decay);
       v.y = fmaf(-lrs, o[4 * q + 1], v.y * decay);
       v.z = fmaf(-lrs, o[4 * q + 2], v.z * decay);
       v.w = fmaf(-lrs, o[4 * q + 3], v.w * decay);
-      w[q] = v;
+      __stcs(w + q, v);
     }
   } else {
 #pragma unroll
@@ -307,10 +307,12 @@ __device__ __forceinline__ bool apply_load_row_run(const ApplyArgs& ap, const Ma
   const long long s0 = g0 / ap.L;
   const long long off0 = g0 - s0 * ap.L;
   if (off0 + 32 <= ap.L && (off0 & 3) == 0) {
+    // Weights are touched once per step: stream them past L2 (evict first) so they do
+    // not push out the X and B panels the tile wave is reusing.
     const float4* src = reinterpret_cast<const float4*>(ap.W.p[s0] + off0);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const float4 v = src[q];
+      const float4 v = __ldcs(src + q);
       w[4 * q + 0] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
     }
     return true;
@@ -337,7 +339,7 @@ __device__ __forceinline__ void apply_store_row_run(const ApplyArgs& ap, const M
     v.y = fmaf(-lrs, o[4 * q + 1], w[4 * q + 1] * decay);
     v.z = fmaf(-lrs, o[4 * q + 2], w[4 * q + 2] * decay);
     v.w = fmaf(-lrs, o[4 * q + 3], w[4 * q + 3] * decay);
-    dst[q] = v;
+    __stcs(dst + q, v);
   }
 }
 

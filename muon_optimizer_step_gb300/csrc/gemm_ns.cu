@@ -1,0 +1,715 @@
+// bf16 Newton-Schulz on the sm_103a tensor cores (tcgen05 + TMEM + TMA): every iteration
+// and phase of the orthogonalization of every matrix of a flat buffer in ONE persistent,
+// cooperative launch.
+//
+// Phases of one iteration (quintic Newton-Schulz, (a, b, c) = (3.4445, -4.7750, 2.0315)):
+//   Gram    A = X X^T           (tall X: A = X^T X)      upper-triangle tiles, mirrored
+//   Poly    B = b*A + c*A A     (A symmetric)            upper-triangle tiles, mirrored
+//   Update  X' = s*(a*X + B X)  (tall X: X' = s*(a*X + X B))
+// s = 1/||X||_F in the first iteration (the Gram epilogue takes s^2), 1 after it.  X keeps
+// its stored row-major orientation; a tall matrix's transposes are MN-major operand reads.
+// The last Update can also apply W <- W*(1 - lr*wd) - lr*sqrt(max(1, r/c))*O from the fp32 O.
+//
+// Scheduling: the host deals each phase's tiles to CTAs (longest first); a CTA walks its
+// lists for iteration 0..n-1, phase Gram, Poly, Update.  A tile starts when the phase it
+// reads is complete *for its own matrix*: per matrix and phase a counter in the workspace
+// counts finished CTA-tiles (release after the epilogue's stores; acquire + an async-proxy
+// fence before the TMA reads).  Matrices therefore flow through the phases independently,
+// and the tail of one phase overlaps the start of the next.  Every CTA's lists are in
+// phase order and all CTAs are co-resident (cooperative launch, one CTA per SM), so some
+// CTA can always progress; every wait is bounded anyway.
+//
+// Two tile shapes share this code:
+//   kPair = false: one CTA per 128 x 256 output tile, tcgen05.mma.cta_group::1, M=128 N=256;
+//   kPair = true:  a 2-CTA cluster per 256 x 256 tile; CTA r loads rows [128r, 128r+128)
+//                  of the A and of the B operand, the even CTA issues
+//                  tcgen05.mma.cta_group::2 (M=256 N=256) over both CTAs' shared memory and
+//                  each CTA drains its own 128 accumulator rows.  A third less operand
+//                  traffic per k-block; used when most of the work sits in big matrices.
+// CTA roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM allocator,
+// warps 4-11 epilogue (two warps per TMEM lane quarter, half the columns each).
+#include <cstdio>
+#include <string>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace muon {
+
+namespace {
+
+constexpr int NUM_THREADS = 384;
+constexpr int EPI_WARPS = 8;
+constexpr int EPI_THREADS = EPI_WARPS * 32;
+constexpr int BK = kTcBK;           // 64 bf16 = one 128-byte swizzle row
+constexpr int BN = 256;             // output tile columns
+constexpr int UMMA_K = 16;
+constexpr int TMEM_COLS = 512;      // two 128 x 256 fp32 accumulators
+constexpr int MN_BOX_BYTES = 64 * BK * 2;
+constexpr float kA = 3.4445f, kB = -4.7750f, kC = 2.0315f;
+
+template <bool kPair>
+struct Cfg {
+  static constexpr int BM = kPair ? 256 : 128;      // output rows per tile
+  static constexpr int BROWS = kPair ? 128 : 256;   // B-operand rows this CTA loads
+  static constexpr int A_BYTES = 128 * BK * 2;      // 16 KB
+  static constexpr int B_BYTES = BROWS * BK * 2;    // 16 KB (pair) / 32 KB (single)
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = kPair ? 7 : 4;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+};
+
+struct NsParams {
+  const TileDev* tiles[3];
+  const int32_t* begin[3];   // per phase: tile-list offsets per CTA (per pair for kPair)
+  const MatDev* mats;
+  const CUtensorMap* tmaps;
+  uint8_t* ws;
+  const float* inv_norm;
+  int* counters;             // per matrix and phase: finished CTA-tiles (zeroed per call)
+  int* err;
+  long long budget;
+  int ns_steps;
+  int q_begin, q_end;        // this launch runs phases q = 3*it + phase in [q_begin, q_end)
+  int apply;                 // last Update also applies the step to W
+  ApplyArgs ap;
+};
+
+// Which tensor maps and transpose bits a tile of `phase` uses.
+struct TileOps {
+  int a_map, b_map;
+  int a_mn, b_mn;
+};
+
+template <bool kPair>
+__device__ __forceinline__ TileOps tile_ops(const MatDev& mt, int phase, int x_in) {
+  const int xk = x_in ? kMapX1K128 : kMapX0K128;
+  const int xkb = kPair ? xk : (x_in ? kMapX1K256 : kMapX0K256);
+  const int xmn = x_in ? kMapX1MN : kMapX0MN;
+  TileOps o;
+  if (phase == kPhaseGram) {
+    if (mt.tall) { o.a_map = xmn; o.b_map = xmn; o.a_mn = 1; o.b_mn = 1; }
+    else { o.a_map = xk; o.b_map = xkb; o.a_mn = 0; o.b_mn = 0; }
+  } else if (phase == kPhasePoly) {
+    o.a_map = kMapAK128; o.b_map = kPair ? kMapAK128 : kMapAK256; o.a_mn = 0; o.b_mn = 0;
+  } else {
+    if (mt.tall) { o.a_map = xk; o.b_map = kPair ? kMapBK128 : kMapBK256; o.a_mn = 0; o.b_mn = 0; }
+    else { o.a_map = kMapBK128; o.b_map = xmn; o.a_mn = 0; o.b_mn = 1; }
+  }
+  return o;
+}
+
+// The counter a tile of (it, phase) waits on, and the value that means "complete".
+__device__ __forceinline__ int dep_slot(const MatDev& mt, int mat, int it, int phase,
+                                        int* target) {
+  if (phase == kPhaseGram) {
+    *target = it * mt.sig[kPhaseUpdate];
+    return mat * 3 + kPhaseUpdate;
+  }
+  *target = (it + 1) * mt.sig[phase - 1];
+  return mat * 3 + phase - 1;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Waits (bounded) until *c >= target; then orders later async-proxy (TMA) reads after the
+// data the counter publishes.
+__device__ __forceinline__ bool wait_counter(const int* c, int target, long long budget, int* err,
+                                             volatile int* abort) {
+  if (target > 0 && ld_acquire_gpu(c) < target) {
+    const long long t0 = clock64();
+    while (ld_acquire_gpu(c) < target) {
+      if (*abort) return false;
+      if (clock64() - t0 > budget) {
+        atomicExch(err, kErrTimeout);
+        *abort = 1;
+        return false;
+      }
+      __nanosleep(128);
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
+__device__ __forceinline__ void signal_counter(int* c) {
+  asm volatile("fence.acq_rel.gpu;\n\tred.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(c) : "memory");
+}
+
+__device__ __forceinline__ void epi_barrier() {
+  asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory");
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&f)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    u.x = pack_bf16x2(f[8 * q + 0], f[8 * q + 1]);
+    u.y = pack_bf16x2(f[8 * q + 2], f[8 * q + 3]);
+    u.z = pack_bf16x2(f[8 * q + 4], f[8 * q + 5]);
+    u.w = pack_bf16x2(f[8 * q + 6], f[8 * q + 7]);
+    reinterpret_cast<uint4*>(dst)[q] = u;
+  }
+}
+
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float (&f)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 u = reinterpret_cast<const uint4*>(src)[q];
+    f[8 * q + 0] = bf16_lo(u.x); f[8 * q + 1] = bf16_hi(u.x);
+    f[8 * q + 2] = bf16_lo(u.y); f[8 * q + 3] = bf16_hi(u.y);
+    f[8 * q + 4] = bf16_lo(u.z); f[8 * q + 5] = bf16_hi(u.z);
+    f[8 * q + 6] = bf16_lo(u.w); f[8 * q + 7] = bf16_hi(u.w);
+  }
+}
+
+// Epilogue of accumulator columns [jb, jb+32) of output row i.
+__device__ __forceinline__ void epilogue_chunk(const NsParams& p, const MatDev& mt, int phase,
+                                               int x_in, bool apply, int i, int jb,
+                                               const uint32_t (&acc)[32], float s) {
+  float f[32];
+  if (phase == kPhaseUpdate) {
+    if (i >= mt.rows || jb >= mt.cols) return;
+    const __nv_bfloat16* xin = reinterpret_cast<const __nv_bfloat16*>(p.ws + (x_in ? mt.x1 : mt.x0));
+    __nv_bfloat16* xout = reinterpret_cast<__nv_bfloat16*>(p.ws + (x_in ? mt.x0 : mt.x1));
+    const int64_t row = (int64_t)i * mt.ldx;
+    if (jb + 32 <= mt.cols) {
+      float x[32];
+      load_bf16x32(xin + row + jb, x);
+      if (apply) {
+        // Issue the weight loads with the X loads, before any store, so that the two
+        // memory round trips of this chunk overlap.
+        float w[32];
+        const bool vec = apply_load_row_run(p.ap, mt, i, jb, w);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) f[t] = s * fmaf(kA, x[t], __uint_as_float(acc[t]));
+        store_bf16x32(xout + row + jb, f);
+        apply_store_row_run(p.ap, mt, i, jb, vec, w, f);
+        return;
+      }
+#pragma unroll
+      for (int t = 0; t < 32; ++t) f[t] = s * fmaf(kA, x[t], __uint_as_float(acc[t]));
+      store_bf16x32(xout + row + jb, f);
+    } else {
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        const int j = jb + t;
+        f[t] = 0.f;
+        if (j < mt.cols) {
+          f[t] = s * fmaf(kA, __bfloat162float(xin[row + j]), __uint_as_float(acc[t]));
+          xout[row + j] = __float2bfloat16_rn(f[t]);
+        }
+      }
+      if (apply) apply_row_run(p.ap, mt, i, jb, mt.cols - jb, f);
+    }
+    return;
+  }
+  // Symmetric outputs (A or B, m x m): write (i, j) for j >= i and its mirror (j, i), so
+  // every element has exactly one writer.
+  if (i >= mt.m || jb + 31 < i || jb >= mt.m) return;
+  __nv_bfloat16* am = reinterpret_cast<__nv_bfloat16*>(p.ws + mt.a);
+  __nv_bfloat16* out = phase == kPhaseGram ? am : reinterpret_cast<__nv_bfloat16*>(p.ws + mt.b);
+  const int64_t row = (int64_t)i * mt.lda;
+  const bool full = (jb + 32 <= mt.m);
+  if (phase == kPhaseGram) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) f[t] = __uint_as_float(acc[t]) * s;
+  } else if (full) {
+    float a[32];
+    load_bf16x32(am + row + jb, a);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) f[t] = fmaf(kB, a[t], kC * __uint_as_float(acc[t]));
+  } else {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      const int j = jb + t;
+      f[t] = j < mt.m ? fmaf(kB, __bfloat162float(am[row + j]), kC * __uint_as_float(acc[t]))
+                      : 0.f;
+    }
+  }
+  if (full && jb >= i) {
+    store_bf16x32(out + row + jb, f);
+  } else {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      const int j = jb + t;
+      if (j >= i && j < mt.m) out[row + j] = __float2bfloat16_rn(f[t]);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < 32; ++t) {
+    const int j = jb + t;
+    if (j > i && j < mt.m) out[(int64_t)j * mt.lda + i] = __float2bfloat16_rn(f[t]);
+  }
+}
+
+// Bounded wait; on expiry also tells the peer CTA of a pair to stop.
+template <bool kPair>
+__device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, const NsParams& p,
+                                          volatile int* abort, uint32_t peer_abort) {
+  if (mbar_wait_bounded(bar, parity, p.budget, p.err, abort)) return true;
+  if (kPair) asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1) : "memory");
+  return false;
+}
+
+// Bounded wait that ignores the abort flag: drains copies and MMAs already in flight.
+__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, long long budget,
+                                           int* err) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > budget) {
+      atomicExch(err, kErrTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Epilogue threads agree on stopping (any thread saw an abort or a failed wait).
+__device__ __forceinline__ bool epi_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(EPI_THREADS)
+      : "memory");
+  return r != 0;
+}
+
+template <bool kPair>
+__global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_constant__ NsParams p) {
+  using C = Cfg<kPair>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int abort_flag;
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* tiles_smem = smem_raw + pad;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tiles_smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* acc_full = bars + 2 * C::STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0: the CTA that issues MMAs
+  const int unit = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const uint32_t peer_abort = kPair ? mapa_shared(smem_u32(&abort_flag), rank ^ 1u) : 0u;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);   // the (even) CTA's arrival with the expected bytes
+      mbar_init(&empty[s], 1);  // the MMA commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], (kPair ? 2 : 1) * EPI_WARPS);
+    }
+    mbar_init(mma_done, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    if (kPair) {
+      tmem_alloc_pair(tmem_slot, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, TMEM_COLS);
+      tmem_relinquish();
+    }
+  }
+  tc_fence_before();
+  if (kPair) cluster_sync(); else __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  volatile int* abort = &abort_flag;
+  // Several phases in this launch: tiles wait on, and publish to, the per-matrix counters.
+  const bool chained = p.q_end - p.q_begin > 1;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t ph = 0;
+      long long nfill = 0;
+      bool ok = true;
+      for (int qq = p.q_begin; qq < p.q_end && ok; ++qq) {
+        const int it = qq / 3, phase = qq % 3;
+        {
+          const int x_in = it & 1;
+          for (int ti = p.begin[phase][unit]; ti < p.begin[phase][unit + 1] && ok; ++ti) {
+            const TileDev tile = p.tiles[phase][ti];
+            const MatDev& mt = p.mats[tile.mat];
+            int target;
+            const int slot = dep_slot(mt, tile.mat, it, phase, &target);
+            // One phase per launch: stream order already made the inputs complete.
+            if (!chained) target = 0;
+            if (!wait_counter(p.counters + slot, target, p.budget, p.err, abort)) {
+              if (kPair)
+                asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1) : "memory");
+              ok = false;
+              break;
+            }
+            const TileOps ops = tile_ops<kPair>(mt, phase, x_in);
+            const CUtensorMap* amap = p.tmaps + (size_t)tile.mat * kMapsPerMat + ops.a_map;
+            const CUtensorMap* bmap = p.tmaps + (size_t)tile.mat * kMapsPerMat + ops.b_map;
+            const int ia = tile.i0 + (kPair ? 128 * (int)rank : 0);
+            const int jr = tile.j0 + (kPair ? 128 * (int)rank : 0);
+            for (int kb = 0; kb < tile.kblocks; ++kb) {
+              if (!wait_role<kPair>(&empty[stage], ph ^ 1u, p, abort, peer_abort)) {
+                ok = false;
+                break;
+              }
+              uint8_t* sa = tiles_smem + stage * C::STAGE_BYTES;
+              uint8_t* sb = sa + C::A_BYTES;
+              const int k0 = kb * BK;
+              if (kPair) {
+                // Only the even CTA arrives, announcing both CTAs' bytes; the odd CTA's
+                // copies may land first (the transaction count dips below zero, which
+                // mbarriers allow; the phase still needs the even CTA's arrival).
+                if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+                const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
+                if (ops.a_mn) {
+                  tma_load_2d_pair(smem_u32(sa), amap, ia, k0, fbar);
+                  tma_load_2d_pair(smem_u32(sa) + MN_BOX_BYTES, amap, ia + 64, k0, fbar);
+                } else {
+                  tma_load_2d_pair(smem_u32(sa), amap, k0, ia, fbar);
+                }
+                if (ops.b_mn) {
+                  tma_load_2d_pair(smem_u32(sb), bmap, jr, k0, fbar);
+                  tma_load_2d_pair(smem_u32(sb) + MN_BOX_BYTES, bmap, jr + 64, k0, fbar);
+                } else {
+                  tma_load_2d_pair(smem_u32(sb), bmap, k0, jr, fbar);
+                }
+              } else {
+                mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                if (ops.a_mn) {
+                  tma_load_2d(sa, amap, ia, k0, &full[stage]);
+                  tma_load_2d(sa + MN_BOX_BYTES, amap, ia + 64, k0, &full[stage]);
+                } else {
+                  tma_load_2d(sa, amap, k0, ia, &full[stage]);
+                }
+                if (ops.b_mn) {
+#pragma unroll
+                  for (int q = 0; q < C::BROWS / 64; ++q)
+                    tma_load_2d(sb + q * MN_BOX_BYTES, bmap, jr + 64 * q, k0, &full[stage]);
+                } else {
+                  tma_load_2d(sb, bmap, k0, jr, &full[stage]);
+                }
+              }
+              ++nfill;
+              if (++stage == C::STAGES) {
+                stage = 0;
+                ph ^= 1u;
+              }
+            }
+          }
+        }
+      }
+      // Every copy issued must land before the block exits (already true unless aborted).
+      // For a pair the even CTA's full barriers count both CTAs' copies.
+      if (rank == 0)
+        for (long long k = nfill - 1; k >= 0 && k >= nfill - C::STAGES; --k)
+          wait_drain(&full[k % C::STAGES], (uint32_t)((k / C::STAGES) & 1), p.budget, p.err);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t ph = 0;
+      int lt = 0;
+      bool ok = true;
+      const uint32_t sbase = smem_u32(tiles_smem);
+      for (int qq = p.q_begin; qq < p.q_end && ok; ++qq) {
+        const int it = qq / 3, phase = qq % 3;
+        {
+          for (int ti = p.begin[phase][unit]; ti < p.begin[phase][unit + 1]; ++ti, ++lt) {
+            const TileDev tile = p.tiles[phase][ti];
+            const MatDev& mt = p.mats[tile.mat];
+            const TileOps ops = tile_ops<kPair>(mt, phase, it & 1);
+            const uint32_t idesc = idesc_bf16(C::BM, BN, ops.a_mn, ops.b_mn);
+            const int ab = lt & 1;
+            if (!wait_role<kPair>(&acc_empty[ab], (uint32_t)(((lt >> 1) & 1) ^ 1), p, abort,
+                                  peer_abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem_base + (uint32_t)(ab * BN);
+            for (int kb = 0; kb < tile.kblocks && ok; ++kb) {
+              if (!wait_role<kPair>(&full[stage], ph, p, abort, peer_abort)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t sa = sbase + stage * C::STAGE_BYTES;
+              const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+              for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                const uint64_t ad = ops.a_mn ? smem_desc_sw128(sa + kk * 2048, MN_BOX_BYTES, 1024)
+                                             : smem_desc_sw128(sa + kk * 32, 16, 1024);
+                const uint64_t bd = ops.b_mn ? smem_desc_sw128(sb + kk * 2048, MN_BOX_BYTES, 1024)
+                                             : smem_desc_sw128(sb + kk * 32, 16, 1024);
+                if (kPair) tc_mma_f16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                else tc_mma_f16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              }
+              if (kPair) tc_commit_pair(&empty[stage], (uint16_t)0x3);
+              else tc_commit(&empty[stage]);
+              if (++stage == C::STAGES) {
+                stage = 0;
+                ph ^= 1u;
+              }
+            }
+            if (!ok) break;
+            if (kPair) tc_commit_pair(&acc_full[ab], (uint16_t)0x3);
+            else tc_commit(&acc_full[ab]);
+          }
+        }
+      }
+      // Every MMA issued must complete before TMEM is released.
+      if (kPair) tc_commit_pair(mma_done, (uint16_t)0x1);
+      else tc_commit(mma_done);
+      wait_drain(mma_done, 0, p.budget, p.err);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- epilogue
+    // Two warps per TMEM lane quarter (warp % 4), each draining half the columns.
+    const int q = warp & 3;
+    const int half = (warp - 4) >> 2;
+    const int r = 32 * q + lane;
+    int lt = 0;
+    bool stop = false;
+    for (int qq = p.q_begin; qq < p.q_end && !stop; ++qq) {
+      const int it = qq / 3, phase = qq % 3;
+      {
+        const int x_in = it & 1;
+        const bool apply = p.apply && phase == kPhaseUpdate && it == p.ns_steps - 1;
+        for (int ti = p.begin[phase][unit]; ti < p.begin[phase][unit + 1]; ++ti, ++lt) {
+          const TileDev tile = p.tiles[phase][ti];
+          const MatDev& mt = p.mats[tile.mat];
+          const int ab = lt & 1;
+          bool ok = *abort == 0 && mbar_wait_bounded(&acc_full[ab], (uint32_t)((lt >> 1) & 1),
+                                                     p.budget, p.err, abort);
+          ok = __all_sync(0xffffffffu, ok);
+          if (ok) {
+            tc_fence_after();
+            // The epilogue reads what the previous phase wrote (A, X): acquire its counter.
+            int target;
+            const int slot = dep_slot(mt, tile.mat, it, phase, &target);
+            if (chained && target > 0) (void)ld_acquire_gpu(p.counters + slot);
+            float s = 1.f;
+            if (it == 0 && phase != kPhasePoly) {
+              const float inv = p.inv_norm[tile.mat];
+              s = phase == kPhaseGram ? inv * inv : inv;
+            }
+            const int i = tile.i0 + (kPair ? 128 * (int)rank : 0) + r;
+#pragma unroll 1
+            for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(
+                  tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * BN + 32 * c), v);
+              tmem_ld_wait();
+              epilogue_chunk(p, mt, phase, x_in, apply, i, tile.j0 + 32 * c, v, s);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (ok && lane == 0) {
+            if (!kPair || rank == 0) mbar_arrive(&acc_empty[ab]);
+            else mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[ab]), 0));
+          }
+          if (chained) {
+            // All epilogue warps stop together, or publish the finished tile together.
+            stop = epi_any(!ok || *abort != 0);
+            if (stop) break;
+            if (warp == 4 && lane == 0) signal_counter(p.counters + tile.mat * 3 + phase);
+          } else if (!ok) {
+            stop = true;
+            break;
+          }
+        }
+      }
+    }
+    if (stop && kPair)
+      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1) : "memory");
+  }
+  tc_fence_before();
+  if (kPair) cluster_sync(); else __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    if (kPair) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+__global__ void selftest_timeout_kernel(int* err, long long budget) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // Nobody arrives on `bar`: the wait must run out, record the timeout and return.
+  if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, budget, err, &abort_flag);
+}
+
+template <bool kPair>
+cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_steps,
+                        int q_begin, int q_end, long long budget, const ApplyArgs* ap,
+                        cudaStream_t st) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  NsParams p;
+  for (int ph = 0; ph < 3; ++ph) {
+    p.tiles[ph] = dt.tiles[ph];
+    p.begin[ph] = dt.cta_begin[ph];
+  }
+  p.mats = dt.mats;
+  p.tmaps = dt.tmaps;
+  p.ws = w;
+  p.inv_norm = reinterpret_cast<const float*>(w + plan.ws_inv_norm);
+  p.counters = reinterpret_cast<int*>(w + plan.ws_counters);
+  p.err = dt.err;
+  p.budget = budget;
+  p.ns_steps = ns_steps;
+  p.q_begin = q_begin;
+  p.q_end = q_end;
+  p.apply = ap != nullptr ? 1 : 0;
+  if (ap != nullptr) p.ap = *ap;
+  cudaError_t e = cudaSuccess;
+  if (q_end - q_begin > 1) {
+    e = cudaMemsetAsync(p.counters, 0, plan.mats.size() * 3 * sizeof(int), st);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((kPair ? 2 : 1) * dt.tc_units), 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<kPair>::SMEM_BYTES;
+  cfg.stream = st;
+  // Cooperative: every CTA must be resident at once, because tiles wait on tiles of
+  // other CTAs.  The grid never exceeds one CTA (pair) per SM (TPC).
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, ns_tc_kernel<kPair>, p);
+  if (e != cudaSuccess && kPair) {
+    // Cluster kernels may not take the cooperative attribute; the grid is sized to the
+    // device's resident-cluster count, so on an otherwise idle GPU all pairs are resident.
+    (void)cudaGetLastError();
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelEx(&cfg, ns_tc_kernel<kPair>, p);
+  }
+  return e;
+}
+
+}  // namespace
+
+cudaError_t prepare_ns_kernels(int* max_pairs) {
+  cudaError_t e = cudaFuncSetAttribute(ns_tc_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg<false>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(ns_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<true>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 1024, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<true>::SMEM_BYTES;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, ns_tc_kernel<true>, &cfg);
+  if (e != cudaSuccess) return e;
+  *max_pairs = n;
+  return cudaSuccess;
+}
+
+cudaError_t launch_ns_tc(const Plan& plan, const DevTables& dt, void* ws, int ns_steps,
+                         long long budget, const ApplyArgs* ap, cudaStream_t st) {
+  if (dt.tc_units == 0 || ns_steps == 0) return cudaSuccess;
+  const int nq = 3 * ns_steps;
+  // Persistent: one launch for every phase; otherwise one launch per phase (the counters
+  // are then satisfied by stream order, and each list is balanced on its own).
+  const int step = dt.tc_persistent ? nq : 1;
+  for (int q0 = 0; q0 < nq; q0 += step) {
+    const cudaError_t e =
+        dt.tc_pair ? launch_impl<true>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
+                   : launch_impl<false>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_selftest_timeout(int* err, long long budget, cudaStream_t st) {
+  selftest_timeout_kernel<<<1, 32, 0, st>>>(err, budget);
+  return cudaGetLastError();
+}
+
+bool encode_tensor_maps(const Plan& plan, const void* ws, std::vector<CUtensorMap>* maps,
+                        std::string* err) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    const cudaError_t e =
+        cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      *err = "cuTensorMapEncodeTiled is not available from the driver";
+      return false;
+    }
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  maps->assign(plan.mats.size() * kMapsPerMat, CUtensorMap{});
+  const uint8_t* base = static_cast<const uint8_t*>(ws);
+  auto make = [&](CUtensorMap* m, int64_t off, uint64_t inner, uint64_t outer, uint64_t pitch,
+                  uint32_t box_inner, uint32_t box_outer) -> bool {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {pitch * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                              const_cast<uint8_t*>(base + off), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      char buf[160];
+      std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed (%d) for a %llux%llu tensor",
+                    (int)r, (unsigned long long)outer, (unsigned long long)inner);
+      *err = buf;
+      return false;
+    }
+    return true;
+  };
+  for (size_t i = 0; i < plan.mats.size(); ++i) {
+    const MatDev& mt = plan.mats[i];
+    CUtensorMap* m = maps->data() + i * kMapsPerMat;
+    const int64_t xs[2] = {mt.x0, mt.x1};
+    for (int b = 0; b < 2; ++b) {
+      if (!make(m + 3 * b + 0, xs[b], mt.cols, mt.rows, mt.ldx, 64, 128)) return false;
+      if (!make(m + 3 * b + 1, xs[b], mt.cols, mt.rows, mt.ldx, 64, 256)) return false;
+      if (!make(m + 3 * b + 2, xs[b], mt.cols, mt.rows, mt.ldx, 64, 64)) return false;
+    }
+    if (!make(m + kMapAK128, mt.a, mt.m, mt.m, mt.lda, 64, 128)) return false;
+    if (!make(m + kMapAK256, mt.a, mt.m, mt.m, mt.lda, 64, 256)) return false;
+    if (!make(m + kMapBK128, mt.b, mt.m, mt.m, mt.lda, 64, 128)) return false;
+    if (!make(m + kMapBK256, mt.b, mt.m, mt.m, mt.lda, 64, 256)) return false;
+  }
+  return true;
+}
+
+}  // namespace muon

@@ -25,8 +25,10 @@ struct DevTables {
   int32_t* cta_begin[3] = {nullptr, nullptr, nullptr};
   int grid[3] = {0, 0, 0};
   CUtensorMap* tmaps = nullptr; // kMapsPerMat per matrix (bf16 path)
-  int tc_variant[3] = {2, 2, 2}; // bf16 path, per phase: 1 = single CTA 128x256 tiles,
-                                 // 2 = CTA pairs 256x256 tiles (grid[] then counts pairs)
+  bool tc_pair = true;          // bf16 path: CTA pairs (256x256 tiles) or single CTAs (128x256)
+  bool tc_persistent = false;   // bf16 path: all phases in one launch (tiles in matrix order)
+  int tc_units = 0;             // bf16 path: CTAs (or pairs) of each launch; every
+                                // phase's cta_begin has tc_units + 1 entries
   const void* tmap_ws = nullptr;  // workspace the tensor maps were encoded for
 };
 
@@ -53,17 +55,12 @@ cudaError_t launch_scatter(const Plan& plan, const DevTables& dt, const float* f
 cudaError_t launch_export(const Plan& plan, const DevTables& dt, const void* ws, int buf,
                           int pending_norm, float* full, cudaStream_t st);
 
-// Stage 2, bf16 path: one tcgen05 GEMM phase over every matrix.
-// With ap != nullptr (last Update only) the epilogue also applies the step to the weights.
-cudaError_t launch_ns_phase_tc(const Plan& plan, const DevTables& dt, void* ws, int phase,
-                               int x_in, int iter0, long long budget, const ApplyArgs* ap,
-                               cudaStream_t st);
-// Stage 2, bf16 path on CTA pairs (tcgen05 cta_group::2): grid[phase] counts pairs.
-cudaError_t launch_ns_phase_tc2(const Plan& plan, const DevTables& dt, void* ws, int phase,
-                                int x_in, int iter0, long long budget, const ApplyArgs* ap,
-                                cudaStream_t st);
-// Shared-memory opt-in of the pair kernel and how many pairs can be resident at once.
-cudaError_t prepare_tc2_kernel(int* max_pairs);
+// Stage 2, bf16 path: all ns_steps iterations of every matrix in one persistent tcgen05
+// launch (with ap != nullptr the last Update also applies the step to the weights).
+cudaError_t launch_ns_tc(const Plan& plan, const DevTables& dt, void* ws, int ns_steps,
+                         long long budget, const ApplyArgs* ap, cudaStream_t st);
+// Shared-memory opt-in of the tcgen05 kernels and how many CTA pairs can be resident.
+cudaError_t prepare_ns_kernels(int* max_pairs);
 // Stage 2, fp32 path: one SIMT GEMM phase over every matrix.
 cudaError_t launch_ns_phase_f32(const Plan& plan, const DevTables& dt, void* ws, int phase,
                                 int x_in, int iter0, cudaStream_t st);
@@ -74,7 +71,5 @@ bool encode_tensor_maps(const Plan& plan, const void* ws, std::vector<CUtensorMa
 cudaError_t launch_selftest_timeout(int* err, long long budget, cudaStream_t st);
 // Sets the message muon_last_error() returns on this thread.
 void set_last_error(const std::string& msg);
-// Prepares the tcgen05 kernel (shared-memory opt-in) on the current device.
-cudaError_t prepare_tc_kernel();
 
 }  // namespace muon

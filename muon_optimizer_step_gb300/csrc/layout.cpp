@@ -129,6 +129,9 @@ std::string build_plan(const int64_t* shapes, const uint8_t* is_matrix, int32_t 
   ws = round_up(ws, 16);
   p.ws_inv_norm = ws;
   ws += (int64_t)p.mats.size() * 4;
+  ws = round_up(ws, 16);
+  p.ws_counters = ws;
+  ws += (int64_t)p.mats.size() * 3 * 4;
   ws = round_up(ws, kWsAlign);
   for (MatDev& m : p.mats) {
     const int64_t xb = round_up((int64_t)m.rows * m.ldx * esz, kWsAlign);
@@ -143,7 +146,8 @@ std::string build_plan(const int64_t* shapes, const uint8_t* is_matrix, int32_t 
   return "";
 }
 
-TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_sms) {
+TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_sms,
+                    bool by_cost) {
   struct Item { TileDev t; int64_t cost; };
   std::vector<Item> items;
   for (size_t mi = 0; mi < plan.mats.size(); ++mi) {
@@ -177,8 +181,9 @@ TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_s
       }
     }
   }
-  std::stable_sort(items.begin(), items.end(),
-                   [](const Item& a, const Item& b) { return a.cost > b.cost; });
+  if (by_cost)
+    std::stable_sort(items.begin(), items.end(),
+                     [](const Item& a, const Item& b) { return a.cost > b.cost; });
   TileList tl;
   if (items.empty() || n_sms <= 0) {
     tl.grid = 0;

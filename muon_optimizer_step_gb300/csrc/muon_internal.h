@@ -48,7 +48,7 @@ struct ChunkDev {          // 32 bytes
   int32_t vec;             // 1: inside one shard, and offsets allow 128-bit accesses
 };
 
-struct MatDev {            // 104 bytes
+struct MatDev {            // 120 bytes
   int32_t rows, cols;      // stored shape
   int32_t m, n;            // min / max of (rows, cols)
   int32_t tall;            // rows > cols: work on X^T (A = X^T X, X' = aX + X B)
@@ -62,6 +62,8 @@ struct MatDev {            // 104 bytes
   float scale;             // sqrt(max(1, rows/cols))
   int32_t group;           // optimizer group (index into per-call hyper-parameters)
   int64_t flat_off;        // element offset of the matrix in the unsharded flat buffer
+  int32_t sig[3];          // per phase: CTA-tiles that signal completion (tcgen05 path)
+  int32_t pad2_;
 };
 
 struct TileDev {           // 16 bytes: one output tile of one GEMM phase
@@ -92,9 +94,11 @@ struct Plan {
   int32_t n_groups = 1;               // optimizer groups (muon_layout_set_groups)
   std::vector<MatDev> mats;           // matrix parameters with numel > 0
   std::vector<ChunkDev> chunks;
-  // Workspace: [partials: n_chunks f32][inv_norm: n_mats f32][per-matrix buffers]
+  // Workspace: [partials: n_chunks f32][inv_norm: n_mats f32][counters: 3 n_mats i32]
+  //            [per-matrix buffers]
   int64_t ws_partials = 0;
   int64_t ws_inv_norm = 0;
+  int64_t ws_counters = 0;            // per matrix and phase: finished tiles (int32)
   int64_t ws_bytes = 0;
 };
 
@@ -102,8 +106,11 @@ struct Plan {
 std::string build_plan(const int64_t* shapes, const uint8_t* is_matrix, int32_t n_params,
                        int32_t n_shards, int32_t ns_dtype, Plan* plan);
 
-// Longest-processing-time assignment of a phase's tiles to `grid` CTAs (grid <= n_sms).
-TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_sms);
+// Assignment of a phase's tiles to `grid` CTAs (grid <= n_sms), each tile to the least
+// loaded CTA: longest first (by_cost), or in matrix order (so that, in a persistent launch,
+// matrices finish a phase one after another and their next phase can start early).
+TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_sms,
+                    bool by_cost = true);
 
 // Owner of every matrix parameter for an n_shards-rank data-parallel group (one shard per
 // rank): longest Newton-Schulz cost first, each to the least-loaded rank among those that

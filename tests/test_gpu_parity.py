@@ -346,10 +346,14 @@ def test_wait_timeout_is_reported_and_context_survives(capi):
 
 
 @pytest.mark.parametrize("variant", ["1", "2"])
-def test_each_tcgen05_variant_vs_oracle(capi, variant, monkeypatch):
-    """Both tcgen05 kernels (single CTA 128x256 tiles, CTA pairs 256x256 tiles), pinned
-    one at a time, on ragged shapes and on a matrix that spans several pair tiles."""
+@pytest.mark.parametrize("persistent", ["0", "1"])
+def test_each_tcgen05_variant_vs_oracle(capi, variant, persistent, monkeypatch):
+    """Both tcgen05 tile shapes (single CTA 128x256 tiles, CTA pairs 256x256 tiles) and
+    both launch modes (one launch per phase; one persistent launch whose tiles wait on
+    per-matrix counters), pinned one at a time, on ragged shapes and on a matrix that
+    spans several pair tiles."""
     monkeypatch.setenv("MUON_TC_KERNEL", variant)
+    monkeypatch.setenv("MUON_NS_PERSISTENT", persistent)
     shapes = [(300, 200), (130, 520), (7, 3), (64, 1000), (257, 129), (600, 1100)]
     wl = inputs.Workload("mixed", tuple(shapes), (True,) * len(shapes), 1, seed=9, rank=4)
     lay = capi.muon_layout_create(wl.shapes, 1, 0, wl.is_matrix)
