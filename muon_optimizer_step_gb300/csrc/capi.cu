@@ -128,10 +128,15 @@ muon_status ensure_device(muon_layout* L) {
       if ((s = upload(tl.cta_begin, &t.cta_begin[p])) != MUON_OK) { free_tables(&t); return s; }
     }
   } else if (!L->plan.mats.empty()) {
-    int pairs = 0;
-    e = prepare_ns_kernels(&pairs);
+    int pairs = 0, singles = 0;
+    e = prepare_ns_kernels(&pairs, &singles);
     if (e != cudaSuccess) { free_tables(&t); return cuda_fail(e, "prepare tcgen05 kernels"); }
     pairs = std::min(pairs, sms / 2);
+    singles = std::min(singles, sms);
+    if (singles < 1) {
+      free_tables(&t);
+      return fail(MUON_ERR_UNSUPPORTED, "the tcgen05 kernel does not fit on an SM of device %d", dev);
+    }
     // CTA pairs (256 x 256 tiles, a third less operand traffic per k-block) when most of
     // the MMA work sits in matrices that span at least ten 256-wide tiles; single CTAs
     // (128 x 256 tiles) otherwise, where the finer tiles balance better.  Measured on
@@ -147,7 +152,7 @@ muon_status ensure_device(muon_layout* L) {
     if (v != nullptr && v[0] == '1') pair = false;
     if (v != nullptr && v[0] == '2' && pairs >= 1) pair = true;
     t.tc_pair = pair;
-    t.tc_units = pair ? pairs : sms;
+    t.tc_units = pair ? pairs : singles;
     // One persistent launch when a phase carries little work (< 100 GFLOP, e.g. the
     // GPT-2-small set: 8% faster there); a launch per phase otherwise (Llama-3-8B: twice as
     // fast as persistent; MoE: 16% faster), where each phase's tiles are balanced alone.

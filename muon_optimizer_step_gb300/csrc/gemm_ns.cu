@@ -26,8 +26,10 @@
 //                  tcgen05.mma.cta_group::2 (M=256 N=256) over both CTAs' shared memory and
 //                  each CTA drains its own 128 accumulator rows.  A third less operand
 //                  traffic per k-block; used when most of the work sits in big matrices.
-// CTA roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM allocator,
-// warps 4-11 epilogue (two warps per TMEM lane quarter, half the columns each).
+// CTA roles (384 threads): warp 0 (lane 0) issues the TMA loads, warp 1 (lane 0) the MMAs,
+// warp 2 allocates TMEM, warps 4-11 drain TMEM (two warps per TMEM lane quarter warp % 4,
+// half the columns each) through the epilogue.  Registers are split per SM sub-partition:
+// three warps of a sub-partition share 16K registers, hence at most 168 per thread.
 #include <cstdio>
 #include <string>
 #include <vector>
@@ -41,7 +43,7 @@ namespace muon {
 
 namespace {
 
-constexpr int NUM_THREADS = 384;
+constexpr int NUM_THREADS = 384;  // 12 warps: producer, MMA issuer, TMEM allocator, idle, 8 epilogue
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr int BK = kTcBK;           // 64 bf16 = one 128-byte swizzle row
@@ -58,8 +60,9 @@ struct Cfg {
   static constexpr int A_BYTES = 128 * BK * 2;      // 16 KB
   static constexpr int B_BYTES = BROWS * BK * 2;    // 16 KB (pair) / 32 KB (single)
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = kPair ? 7 : 4;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int STAGES = kPair ? 6 : 4;
+  // operand stages, 4 KB of epilogue staging per epilogue warp, alignment, barriers
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * 4096 + 1024 + 256;
 };
 
 struct NsParams {
@@ -143,111 +146,154 @@ __device__ __forceinline__ void signal_counter(int* c) {
   asm volatile("fence.acq_rel.gpu;\n\tred.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(c) : "memory");
 }
 
-__device__ __forceinline__ void epi_barrier() {
-  asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory");
-}
-
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&f)[32]) {
+__device__ __forceinline__ void unpack_bf16x32(const uint4 (&u)[4], float (&f)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    uint4 u;
-    u.x = pack_bf16x2(f[8 * q + 0], f[8 * q + 1]);
-    u.y = pack_bf16x2(f[8 * q + 2], f[8 * q + 3]);
-    u.z = pack_bf16x2(f[8 * q + 4], f[8 * q + 5]);
-    u.w = pack_bf16x2(f[8 * q + 6], f[8 * q + 7]);
-    reinterpret_cast<uint4*>(dst)[q] = u;
+    f[8 * q + 0] = bf16_lo(u[q].x); f[8 * q + 1] = bf16_hi(u[q].x);
+    f[8 * q + 2] = bf16_lo(u[q].y); f[8 * q + 3] = bf16_hi(u[q].y);
+    f[8 * q + 4] = bf16_lo(u[q].z); f[8 * q + 5] = bf16_hi(u[q].z);
+    f[8 * q + 6] = bf16_lo(u[q].w); f[8 * q + 7] = bf16_hi(u[q].w);
   }
 }
 
-__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float (&f)[32]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 u = reinterpret_cast<const uint4*>(src)[q];
-    f[8 * q + 0] = bf16_lo(u.x); f[8 * q + 1] = bf16_hi(u.x);
-    f[8 * q + 2] = bf16_lo(u.y); f[8 * q + 3] = bf16_hi(u.y);
-    f[8 * q + 4] = bf16_lo(u.z); f[8 * q + 5] = bf16_hi(u.z);
-    f[8 * q + 6] = bf16_lo(u.w); f[8 * q + 7] = bf16_hi(u.w);
-  }
-}
-
-// Epilogue of accumulator columns [jb, jb+32) of output row i.
-__device__ __forceinline__ void epilogue_chunk(const NsParams& p, const MatDev& mt, int phase,
-                                               int x_in, bool apply, int i, int jb,
-                                               const uint32_t (&acc)[32], float s) {
-  float f[32];
+// The global input an epilogue chunk needs besides the accumulator (X for Update, A for
+// Poly), loaded one chunk ahead so that its memory latency overlaps the previous chunk.
+// Returns false when the chunk needs none or takes the element-by-element path.
+__device__ __forceinline__ bool epilogue_prefetch(const NsParams& p, const MatDev& mt, int phase,
+                                                  int x_in, int i, int jb, uint4 (&in)[4]) {
+  const uint4* src;
   if (phase == kPhaseUpdate) {
-    if (i >= mt.rows || jb >= mt.cols) return;
+    if (i >= mt.rows || jb + 32 > mt.cols) return false;
+    src = reinterpret_cast<const uint4*>(p.ws + (x_in ? mt.x1 : mt.x0) +
+                                         2 * ((int64_t)i * mt.ldx + jb));
+  } else if (phase == kPhasePoly) {
+    if (i >= mt.m || jb + 32 > mt.m || jb + 31 < i) return false;
+    src = reinterpret_cast<const uint4*>(p.ws + mt.a + 2 * ((int64_t)i * mt.lda + jb));
+  } else {
+    return false;
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) in[q] = src[q];
+  return true;
+}
+
+// Per-warp staging of one 32 x 32 output block (and its transposed mirror) in shared
+// memory, laid out as the 64-byte-swizzled boxes the TMA stores read: element (row r,
+// column c) of a block sits at byte 64 r + 16 ((c / 8) ^ ((r / 2) % 4)) + 2 (c % 8).
+struct EpiStage {
+  uint8_t* dir;   // 2 KB, 512-byte aligned
+  uint8_t* mir;   // 2 KB
+  bool pending;   // a bulk store may still be reading these buffers (tracked by lane 0)
+};
+
+__device__ __forceinline__ uint32_t swz64(int r, int c) {
+  return (uint32_t)(64 * r + 16 * ((c >> 3) ^ ((r >> 1) & 3)) + 2 * (c & 7));
+}
+
+// Epilogue of the 32 x 32 block: rows r0 .. r0+31 (lane = row - r0), accumulator columns
+// [jb, jb+32).  `in` holds the prefetched X or A row segment when have_in.  Full blocks
+// leave through TMA bulk stores (direct block, and its mirror for the symmetric outputs);
+// blocks on the diagonal of a symmetric output keep the element rule (j >= i written,
+// j > i mirrored) so that every element has exactly one writer.
+__device__ __forceinline__ void epilogue_block(const NsParams& p, const MatDev& mt, int mat,
+                                               int phase, int x_in, bool apply, int r0, int jb,
+                                               int lane, const uint32_t (&acc)[32], float s,
+                                               const uint4 (&in)[4], bool have_in,
+                                               EpiStage& st) {
+  const int i = r0 + lane;
+  float f[32];
+  const CUtensorMap* maps = p.tmaps + (size_t)mat * kMapsPerMat;
+  const CUtensorMap* out_map;
+  bool mirror = false;
+  if (phase == kPhaseUpdate) {
+    if (r0 >= mt.rows || jb >= mt.cols) return;  // warp-uniform
     const __nv_bfloat16* xin = reinterpret_cast<const __nv_bfloat16*>(p.ws + (x_in ? mt.x1 : mt.x0));
-    __nv_bfloat16* xout = reinterpret_cast<__nv_bfloat16*>(p.ws + (x_in ? mt.x0 : mt.x1));
     const int64_t row = (int64_t)i * mt.ldx;
-    if (jb + 32 <= mt.cols) {
-      float x[32];
-      load_bf16x32(xin + row + jb, x);
-      if (apply) {
-        // Issue the weight loads with the X loads, before any store, so that the two
-        // memory round trips of this chunk overlap.
-        float w[32];
-        const bool vec = apply_load_row_run(p.ap, mt, i, jb, w);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) f[t] = s * fmaf(kA, x[t], __uint_as_float(acc[t]));
-        store_bf16x32(xout + row + jb, f);
-        apply_store_row_run(p.ap, mt, i, jb, vec, w, f);
-        return;
-      }
-#pragma unroll
-      for (int t = 0; t < 32; ++t) f[t] = s * fmaf(kA, x[t], __uint_as_float(acc[t]));
-      store_bf16x32(xout + row + jb, f);
+    float x[32];
+    if (have_in) {
+      unpack_bf16x32(in, x);
     } else {
 #pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        const int j = jb + t;
-        f[t] = 0.f;
-        if (j < mt.cols) {
-          f[t] = s * fmaf(kA, __bfloat162float(xin[row + j]), __uint_as_float(acc[t]));
-          xout[row + j] = __float2bfloat16_rn(f[t]);
+      for (int t = 0; t < 32; ++t)
+        x[t] = (i < mt.rows && jb + t < mt.cols) ? __bfloat162float(xin[row + jb + t]) : 0.f;
+    }
+    if (apply && i < mt.rows) {
+      // Issue the weight loads before any store so that the round trips overlap.
+      float w[32];
+      const int n = min(32, mt.cols - jb);
+      const bool vec = n == 32 && apply_load_row_run(p.ap, mt, i, jb, w);
+#pragma unroll
+      for (int t = 0; t < 32; ++t) f[t] = s * fmaf(kA, x[t], __uint_as_float(acc[t]));
+      if (vec) apply_store_row_run(p.ap, mt, i, jb, true, w, f);
+      else apply_row_run(p.ap, mt, i, jb, n, f);
+    } else {
+#pragma unroll
+      for (int t = 0; t < 32; ++t) f[t] = s * fmaf(kA, x[t], __uint_as_float(acc[t]));
+    }
+    out_map = maps + (x_in ? kMapX0St : kMapX1St);
+  } else {
+    if (r0 >= mt.m || jb >= mt.m || jb < r0) return;  // outside, or below the diagonal
+    __nv_bfloat16* am = reinterpret_cast<__nv_bfloat16*>(p.ws + mt.a);
+    const int64_t row = (int64_t)i * mt.lda;
+    if (phase == kPhaseGram) {
+#pragma unroll
+      for (int t = 0; t < 32; ++t) f[t] = __uint_as_float(acc[t]) * s;
+    } else {
+      float a[32];
+      if (have_in) {
+        unpack_bf16x32(in, a);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          a[t] = (i < mt.m && jb + t < mt.m) ? __bfloat162float(am[row + jb + t]) : 0.f;
+      }
+#pragma unroll
+      for (int t = 0; t < 32; ++t) f[t] = fmaf(kB, a[t], kC * __uint_as_float(acc[t]));
+    }
+    if (jb == r0) {
+      // Diagonal block: element rule with plain stores.
+      __nv_bfloat16* out = phase == kPhaseGram ? am : reinterpret_cast<__nv_bfloat16*>(p.ws + mt.b);
+      if (i < mt.m) {
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          const int j = jb + t;
+          if (j >= i && j < mt.m) out[row + j] = __float2bfloat16_rn(f[t]);
+          if (j > i && j < mt.m) out[(int64_t)j * mt.lda + i] = __float2bfloat16_rn(f[t]);
         }
       }
-      if (apply) apply_row_run(p.ap, mt, i, jb, mt.cols - jb, f);
+      return;
     }
-    return;
+    out_map = maps + (phase == kPhaseGram ? kMapASt : kMapBSt);
+    mirror = true;
   }
-  // Symmetric outputs (A or B, m x m): write (i, j) for j >= i and its mirror (j, i), so
-  // every element has exactly one writer.
-  if (i >= mt.m || jb + 31 < i || jb >= mt.m) return;
-  __nv_bfloat16* am = reinterpret_cast<__nv_bfloat16*>(p.ws + mt.a);
-  __nv_bfloat16* out = phase == kPhaseGram ? am : reinterpret_cast<__nv_bfloat16*>(p.ws + mt.b);
-  const int64_t row = (int64_t)i * mt.lda;
-  const bool full = (jb + 32 <= mt.m);
-  if (phase == kPhaseGram) {
-#pragma unroll
-    for (int t = 0; t < 32; ++t) f[t] = __uint_as_float(acc[t]) * s;
-  } else if (full) {
-    float a[32];
-    load_bf16x32(am + row + jb, a);
-#pragma unroll
-    for (int t = 0; t < 32; ++t) f[t] = fmaf(kB, a[t], kC * __uint_as_float(acc[t]));
-  } else {
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      const int j = jb + t;
-      f[t] = j < mt.m ? fmaf(kB, __bfloat162float(am[row + j]), kC * __uint_as_float(acc[t]))
-                      : 0.f;
-    }
-  }
-  if (full && jb >= i) {
-    store_bf16x32(out + row + jb, f);
-  } else {
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      const int j = jb + t;
-      if (j >= i && j < mt.m) out[row + j] = __float2bfloat16_rn(f[t]);
-    }
+  // Full block through shared memory and TMA (out-of-range rows / columns are clipped by
+  // the tensor map, so their values do not matter).
+  if (st.pending) {
+    if (lane == 0) bulk_wait_read();
+    __syncwarp();
   }
 #pragma unroll
-  for (int t = 0; t < 32; ++t) {
-    const int j = jb + t;
-    if (j > i && j < mt.m) out[(int64_t)j * mt.lda + i] = __float2bfloat16_rn(f[t]);
+  for (int k = 0; k < 4; ++k) {
+    uint4 u;
+    u.x = pack_bf16x2(f[8 * k + 0], f[8 * k + 1]);
+    u.y = pack_bf16x2(f[8 * k + 2], f[8 * k + 3]);
+    u.z = pack_bf16x2(f[8 * k + 4], f[8 * k + 5]);
+    u.w = pack_bf16x2(f[8 * k + 6], f[8 * k + 7]);
+    *reinterpret_cast<uint4*>(st.dir + swz64(lane, 8 * k)) = u;
   }
+  if (mirror) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+      *reinterpret_cast<__nv_bfloat16*>(st.mir + swz64(t, lane)) = __float2bfloat16_rn(f[t]);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(out_map, jb, r0, smem_u32(st.dir));
+    if (mirror) tma_store_2d(out_map, r0, jb, smem_u32(st.mir));
+    bulk_commit();
+  }
+  st.pending = true;
 }
 
 // Bounded wait; on expiry also tells the peer CTA of a pair to stop.
@@ -293,7 +339,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
   __shared__ int abort_flag;
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* tiles_smem = smem_raw + pad;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(tiles_smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tiles_smem + C::STAGES * C::STAGE_BYTES +
+                                               EPI_WARPS * 4096);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
   uint64_t* acc_full = bars + 2 * C::STAGES;
@@ -488,9 +535,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
     // Two warps per TMEM lane quarter (warp % 4), each draining half the columns.
     const int q = warp & 3;
     const int half = (warp - 4) >> 2;
-    const int r = 32 * q + lane;
     int lt = 0;
     bool stop = false;
+    EpiStage est;
+    est.dir = tiles_smem + C::STAGES * C::STAGE_BYTES + (warp - 4) * 4096;
+    est.mir = est.dir + 2048;
+    est.pending = false;
     for (int qq = p.q_begin; qq < p.q_end && !stop; ++qq) {
       const int it = qq / 3, phase = qq % 3;
       {
@@ -514,14 +564,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
               const float inv = p.inv_norm[tile.mat];
               s = phase == kPhaseGram ? inv * inv : inv;
             }
-            const int i = tile.i0 + (kPair ? 128 * (int)rank : 0) + r;
+            const int r0 = tile.i0 + (kPair ? 128 * (int)rank : 0) + 32 * q;
+            const int i = r0 + lane;
+            const int c_first = half * (BN / 64), c_last = (half + 1) * (BN / 64);
 #pragma unroll 1
-            for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
+            for (int c = c_first; c < c_last; ++c) {
+              uint4 in_cur[4];
+              const bool have_cur = epilogue_prefetch(p, mt, phase, x_in, i, tile.j0 + 32 * c,
+                                                      in_cur);
               uint32_t v[32];
               tmem_ld_32x32b_x32(
                   tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * BN + 32 * c), v);
               tmem_ld_wait();
-              epilogue_chunk(p, mt, phase, x_in, apply, i, tile.j0 + 32 * c, v, s);
+              epilogue_block(p, mt, tile.mat, phase, x_in, apply, r0, tile.j0 + 32 * c, lane, v, s,
+                             in_cur, have_cur, est);
             }
           }
           tc_fence_before();
@@ -531,6 +587,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
             else mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[ab]), 0));
           }
           if (chained) {
+            // The tile's bulk stores must have landed before it is published.
+            if (est.pending) {
+              if (lane == 0) {
+                bulk_wait_all();
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+              }
+              __syncwarp();
+              est.pending = false;
+            }
             // All epilogue warps stop together, or publish the finished tile together.
             stop = epi_any(!ok || *abort != 0);
             if (stop) break;
@@ -544,6 +609,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
     }
     if (stop && kPair)
       asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1) : "memory");
+    // Shared memory must outlive every bulk store that reads it.
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   tc_fence_before();
   if (kPair) cluster_sync(); else __syncthreads();
@@ -619,14 +687,23 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
 
 }  // namespace
 
-cudaError_t prepare_ns_kernels(int* max_pairs) {
-  cudaError_t e = cudaFuncSetAttribute(ns_tc_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg<false>::SMEM_BYTES);
+cudaError_t prepare_ns_kernels(int* max_pairs, int* max_singles) {
+  for (int k = 0; k < 2; ++k) {
+    const void* fn = k == 0 ? (const void*)ns_tc_kernel<false> : (const void*)ns_tc_kernel<true>;
+    const int smem = k == 0 ? Cfg<false>::SMEM_BYTES : Cfg<true>::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  int per_sm = 0, sms = 0, dev = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, ns_tc_kernel<false>, NUM_THREADS, Cfg<false>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(ns_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<true>::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  *max_singles = per_sm * sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * 1024, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
@@ -676,14 +753,15 @@ bool encode_tensor_maps(const Plan& plan, const void* ws, std::vector<CUtensorMa
   maps->assign(plan.mats.size() * kMapsPerMat, CUtensorMap{});
   const uint8_t* base = static_cast<const uint8_t*>(ws);
   auto make = [&](CUtensorMap* m, int64_t off, uint64_t inner, uint64_t outer, uint64_t pitch,
-                  uint32_t box_inner, uint32_t box_outer) -> bool {
+                  uint32_t box_inner, uint32_t box_outer,
+                  CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) -> bool {
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {pitch * 2};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                               const_cast<uint8_t*>(base + off), dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -708,6 +786,11 @@ bool encode_tensor_maps(const Plan& plan, const void* ws, std::vector<CUtensorMa
     if (!make(m + kMapAK256, mt.a, mt.m, mt.m, mt.lda, 64, 256)) return false;
     if (!make(m + kMapBK128, mt.b, mt.m, mt.m, mt.lda, 64, 128)) return false;
     if (!make(m + kMapBK256, mt.b, mt.m, mt.m, mt.lda, 64, 256)) return false;
+    const CUtensorMapSwizzle s64 = CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!make(m + kMapX0St, mt.x0, mt.cols, mt.rows, mt.ldx, 32, 32, s64)) return false;
+    if (!make(m + kMapX1St, mt.x1, mt.cols, mt.rows, mt.ldx, 32, 32, s64)) return false;
+    if (!make(m + kMapASt, mt.a, mt.m, mt.m, mt.lda, 32, 32, s64)) return false;
+    if (!make(m + kMapBSt, mt.b, mt.m, mt.m, mt.lda, 32, 32, s64)) return false;
   }
   return true;
 }

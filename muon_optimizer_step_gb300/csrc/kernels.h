@@ -59,8 +59,9 @@ cudaError_t launch_export(const Plan& plan, const DevTables& dt, const void* ws,
 // launch (with ap != nullptr the last Update also applies the step to the weights).
 cudaError_t launch_ns_tc(const Plan& plan, const DevTables& dt, void* ws, int ns_steps,
                          long long budget, const ApplyArgs* ap, cudaStream_t st);
-// Shared-memory opt-in of the tcgen05 kernels and how many CTA pairs can be resident.
-cudaError_t prepare_ns_kernels(int* max_pairs);
+// Shared-memory opt-in of the tcgen05 kernels and how many CTA pairs / single CTAs can be
+// resident at once.
+cudaError_t prepare_ns_kernels(int* max_pairs, int* max_singles);
 // Stage 2, fp32 path: one SIMT GEMM phase over every matrix.
 cudaError_t launch_ns_phase_f32(const Plan& plan, const DevTables& dt, void* ws, int phase,
                                 int x_in, int iter0, cudaStream_t st);

@@ -34,7 +34,9 @@ enum MapSlot {
   kMapX1K128 = 3, kMapX1K256 = 4, kMapX1MN = 5,
   kMapAK128 = 6, kMapAK256 = 7,
   kMapBK128 = 8, kMapBK256 = 9,
-  kMapsPerMat = 10
+  // 32 x 32 boxes with 64-byte swizzle for the epilogue's TMA stores
+  kMapX0St = 10, kMapX1St = 11, kMapASt = 12, kMapBSt = 13,
+  kMapsPerMat = 14
 };
 
 enum Phase { kPhaseGram = 0, kPhasePoly = 1, kPhaseUpdate = 2 };
