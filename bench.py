@@ -58,32 +58,36 @@ def elementwise_bytes(n_matrix_elems, ns_dtype):
     return n_matrix_elems * (12 + x), n_matrix_elems * (8 + x)
 
 
-# DRAM bytes per Newton-Schulz launch (mean over Gram / Poly / Update) measured with ncu
-# on two Llama-3-8B layers and scaled by 16 to the 32-layer set (profiles/
-# ns_phase_tc2_llama3_8b_x2.md), valid only for the kernel sources it was taken with.
+# DRAM bytes per Newton-Schulz launch (mean over the 15 launches of one step: Gram, Poly,
+# Update x 5, the last Update also applying W), measured with ncu on two Llama-3-8B layers
+# with the same kernel shape and scaled by 16 to the 32-layer set (profiles/
+# ns_tc_kernels_llama3_8b_x2.md).  Valid only for the kernel shape and the sources it was
+# taken with.
 NS_TRAFFIC = {
-    "llama3_8b_x32": {"bytes_per_launch": 16 * (1643911680 + 308051200 + 393551616 + 301336832
-                                                + 1937092352 + 840659712) / 3,
-                      "sources_sha256": "f6526958530d68364d2649d541e6b0ea1706db09ebc38f81b90bd1fcb22a7cdd"
-                                        "4a62cde6d76fdc1497b832035d8dcc9600b51a7c28220f28889df8a0430e42ae"
-                                        "2108b28e80686f6387a0970aac095580cb0cd4e61b4e7650c1da99dcdd7d86f0"},
+    "llama3_8b_x32": {"bytes_per_launch": 16 * (21402986496 + 9351046912) / 15,
+                      "cta_pair": False,
+                      "sources_sha256": "c38ac66a52445128f7dd0ff5b37e9089e869439dfb4374ab63f6dfcd4d01472f"},
 }
+NS_SOURCES = ("gemm_ns.cu", "device_common.cuh", "layout.cpp")
 
 
 def _ns_sources_sha256():
     import hashlib
-    out = ""
-    for f in ("gemm_tc2.cu", "gemm_tc.cu", "layout.cpp"):
+    h = hashlib.sha256()
+    for f in NS_SOURCES:
         with open(os.path.join(ROOT, "muon_optimizer_step_gb300", "csrc", f), "rb") as fh:
-            out += hashlib.sha256(fh.read()).hexdigest()
-    return out
+            h.update(fh.read())
+    return h.hexdigest()
 
 
-def ns_traffic(workload, ns_dtype):
+def ns_traffic(workload, ns_dtype, kernel):
     """Measured DRAM bytes per Newton-Schulz launch, or None if not measured for this
-    workload or if the kernel sources changed since the counters were taken."""
+    workload and kernel shape, or if the kernel sources changed since the counters were
+    taken."""
     rec = NS_TRAFFIC.get(workload)
-    if rec is None or ns_dtype != "bf16":
+    if rec is None or ns_dtype != "bf16" or kernel is None:
+        return None
+    if kernel["cta_pair"] != rec["cta_pair"]:
         return None
     try:
         if _ns_sources_sha256() != rec["sources_sha256"]:
@@ -91,6 +95,16 @@ def ns_traffic(workload, ns_dtype):
     except OSError:
         return None
     return rec["bytes_per_launch"]
+
+
+def ns_kernel_label(kernel, ns_steps):
+    if kernel is None:
+        return "ns_phase_f32_kernel (fp32 CUDA cores, 3 launches per iteration)"
+    name = "ns_tc_pair_kernel (tcgen05 cta_group::2, 256x256 tiles)" if kernel["cta_pair"] \
+        else "ns_tc_single_kernel (tcgen05 cta_group::1, 128x256 tiles)"
+    launches = 1 if kernel["persistent"] else 3 * ns_steps
+    return "%s, %d units, %d launch(es) per step; the last Update also applies W" % (
+        name, kernel["units"], launches)
 
 
 def load_peaks():
@@ -307,6 +321,7 @@ def run_ours(args):
     ns_dtype = capi.MUON_NS_BF16 if args.ns_dtype == "bf16" else capi.MUON_NS_FP32
     ns_steps = wl.ns_steps
     lay = capi.muon_layout_create(wl.shapes, wl.n_shards, ns_dtype, wl.is_matrix)
+    ns_kernel = capi.muon_layout_ns_kernel(lay) if ns_dtype == capi.MUON_NS_BF16 else None
     S, L, N = wl.n_shards, lay.shard_len, lay.numel
     # One allocation per buffer; shard s is a view of [s*L, (s+1)*L), the first N elements
     # are the unsharded flat buffer.
@@ -462,8 +477,11 @@ def run_ours(args):
         peak_tc = props.multi_processor_count * 128 * 2 * 2070e6 / 1e12
         peak_note = "derived fp32 CUDA-core peak: %d SMs x 128 lanes x 2 flops x 2070 MHz" % (
             props.multi_processor_count)
-    launches_per_step = (2 + 3 * ns_steps + (0 if (args.ns_dtype == "bf16" and ns_steps >= 1)
-                                             else 1)) if n_mat_elems else 0
+    ns_launches = (1 if ns_kernel is not None and ns_kernel["persistent"] else 3 * ns_steps) \
+        if ns_steps >= 1 else 0
+    # stage 1 (momentum + norm finalize), the Newton-Schulz launches, and the apply pass
+    # unless the last Update applies W
+    launches_per_step = (2 + ns_launches + (0 if fused_tail else 1)) if n_mat_elems else 0
     line = {
         "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
@@ -480,12 +498,10 @@ def run_ours(args):
         "stage_ms": {"momentum_inputs": stage_ms[0], "orthogonalize_apply": stage_ms[1]},
         "fused_apply": fused_tail,
         "roofline": {"bound": "tensor" if args.ns_dtype == "bf16" else "alu",
-                     "kernel": "tcgen05 Newton-Schulz phase kernels (3 per iteration, "
-                               "%d launches per step; the last one also applies the "
-                               "update to W)" % (3 * ns_steps),
+                     "kernel": ns_kernel_label(ns_kernel, ns_steps),
                      "achieved": ns_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": ns_tflops / peak_tc,
-                     "traffic": ns_traffic(wl.name, args.ns_dtype),
+                     "traffic": ns_traffic(wl.name, args.ns_dtype, ns_kernel),
                      "traffic_unit": "DRAM bytes per launch (ncu, mean over phases)",
                      "peak_note": peak_note},
         "roofline_elementwise": {"bound": "hbm", "kernel": "momentum_input_kernel",

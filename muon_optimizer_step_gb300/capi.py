@@ -69,6 +69,8 @@ SIGNATURES = [
     ("muon_orthogonalize_full_noalloc", _I32, [_P, _P, _P, _I32, _P]),
     ("muon_check", _I32, [_P]),
     ("muon_selftest_wait_timeout", _I32, [_I64, _P]),
+    ("muon_layout_ns_kernel", _I32, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32),
+                                     ctypes.POINTER(_I32)]),
 ]
 
 
@@ -317,6 +319,16 @@ def muon_check_status(stream=None) -> int:
 def muon_selftest_wait_timeout(budget_cycles, stream=None):
     _check(lib.muon_selftest_wait_timeout(int(budget_cycles), _stream_handle(stream)),
            "muon_selftest_wait_timeout")
+
+
+def muon_layout_ns_kernel(layout) -> dict:
+    """The Newton-Schulz kernel `layout` runs on the current device:
+    {"cta_pair": bool, "units": int, "persistent": bool}."""
+    pair, units, pers = _I32(), _I32(), _I32()
+    _check(lib.muon_layout_ns_kernel(layout.handle, ctypes.byref(pair), ctypes.byref(units),
+                                     ctypes.byref(pers)), "muon_layout_ns_kernel")
+    return {"cta_pair": bool(pair.value), "units": int(units.value),
+            "persistent": bool(pers.value)}
 
 
 def muon_last_error() -> str:

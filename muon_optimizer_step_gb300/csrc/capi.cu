@@ -137,20 +137,28 @@ muon_status ensure_device(muon_layout* L) {
       free_tables(&t);
       return fail(MUON_ERR_UNSUPPORTED, "the tcgen05 kernel does not fit on an SM of device %d", dev);
     }
-    // CTA pairs (256 x 256 tiles, a third less operand traffic per k-block) when most of
-    // the MMA work sits in matrices that span at least ten 256-wide tiles; single CTAs
-    // (128 x 256 tiles) otherwise, where the finer tiles balance better.  Measured on
-    // GB300: pairs 4-7% faster on the Llama-3-8B set, 7-10% slower on GPT-2 and MoE.
-    double big = 0.0, all = 0.0;
-    for (const MatDev& m : L->plan.mats) {
-      const double work = 3.0 * m.m * (double)m.m * m.n + (double)m.m * m.m * m.m;
-      all += work;
-      if (m.m >= 2560) big += work;
-    }
-    bool pair = pairs >= 1 && big >= 0.5 * all;
+    // CTA pairs (256 x 256 tiles) keep the tensor pipe busier per clock (74-76% of active
+    // cycles against 71% for single CTAs on two Llama-3-8B layers) and are 3-6% faster on
+    // the GPT-2, MoE and two-layer sets.  They also draw more power per clock, so a buffer
+    // whose steps run long enough to hold the GPU at its power limit runs single CTAs
+    // (128 x 256 tiles) at ~6% higher clocks: 1.3% faster on the Llama-3-8B set at 1.4 kW.
+    // The cut is the Newton-Schulz work of one iteration: 94 TFLOP on that set, 6 on the
+    // two-layer one.
+    double all = 0.0;  // flops of one iteration, symmetric count: 3 m^2 n + m^3 per matrix
+    for (const MatDev& m : L->plan.mats)
+      all += 3.0 * m.m * (double)m.m * m.n + (double)m.m * m.m * m.m;
+    bool pair = pairs >= 1 && all < 20e12;
     const char* v = std::getenv("MUON_TC_KERNEL");  // "1" / "2" pins a shape (measurements)
     if (v != nullptr && v[0] == '1') pair = false;
-    if (v != nullptr && v[0] == '2' && pairs >= 1) pair = true;
+    if (v != nullptr && v[0] == '2') {
+      if (pairs < 1) {
+        free_tables(&t);
+        return fail(MUON_ERR_UNSUPPORTED,
+                    "MUON_TC_KERNEL=2 asks for CTA pairs, but no 2-CTA cluster of the tcgen05 "
+                    "kernel fits on device %d", dev);
+      }
+      pair = true;
+    }
     t.tc_pair = pair;
     t.tc_units = pair ? pairs : singles;
     // One persistent launch when a phase carries little work (< 100 GFLOP, e.g. the
@@ -625,6 +633,20 @@ muon_status muon_check(cudaStream_t stream) {
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "pending CUDA error");
+  return ok();
+}
+
+muon_status muon_layout_ns_kernel(const muon_layout* layout, int32_t* cta_pair, int32_t* units,
+                                  int32_t* persistent) {
+  if (layout == nullptr || cta_pair == nullptr || units == nullptr || persistent == nullptr)
+    return fail(MUON_ERR_INVALID_ARG, "null argument");
+  muon_layout* L = const_cast<muon_layout*>(layout);
+  std::lock_guard<std::mutex> guard(L->mu);
+  MUON_TRY(ensure_device(L));
+  const bool tc = L->plan.ns_dtype == MUON_NS_BF16 && !L->plan.mats.empty();
+  *cta_pair = tc && L->dt.tc_pair ? 1 : 0;
+  *units = tc ? L->dt.tc_units : 0;
+  *persistent = tc && L->dt.tc_persistent ? 1 : 0;
   return ok();
 }
 

@@ -1,6 +1,6 @@
-// bf16 Newton-Schulz on the sm_103a tensor cores (tcgen05 + TMEM + TMA): every iteration
-// and phase of the orthogonalization of every matrix of a flat buffer in ONE persistent,
-// cooperative launch.
+// bf16 Newton-Schulz on the sm_103a tensor cores (tcgen05 + TMEM + TMA): the phases of
+// every matrix of a flat buffer as grouped launches, one per phase, or all of them in one
+// persistent, cooperative launch (small buffers).
 //
 // Phases of one iteration (quintic Newton-Schulz, (a, b, c) = (3.4445, -4.7750, 2.0315)):
 //   Gram    A = X X^T           (tall X: A = X^T X)      upper-triangle tiles, mirrored
@@ -20,8 +20,8 @@
 // CTA can always progress; every wait is bounded anyway.
 //
 // Two tile shapes share this code:
-//   kPair = false: one CTA per 128 x 256 output tile, tcgen05.mma.cta_group::1, M=128 N=256;
-//   kPair = true:  a 2-CTA cluster per 256 x 256 tile; CTA r loads rows [128r, 128r+128)
+//   ns_tc_single_kernel: one CTA per 128 x 256 output tile, tcgen05.mma.cta_group::1, M=128 N=256;
+//   ns_tc_pair_kernel: a 2-CTA cluster per 256 x 256 tile; CTA r loads rows [128r, 128r+128)
 //                  of the A and of the B operand, the even CTA issues
 //                  tcgen05.mma.cta_group::2 (M=256 N=256) over both CTAs' shared memory and
 //                  each CTA drains its own 128 accumulator rows.  A third less operand
@@ -333,7 +333,7 @@ __device__ __forceinline__ bool epi_any(bool v) {
 }
 
 template <bool kPair>
-__global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_constant__ NsParams p) {
+__device__ __forceinline__ void ns_tc_body(const NsParams& p) {
   using C = Cfg<kPair>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
@@ -622,6 +622,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_tc_kernel(const __grid_cons
   }
 }
 
+// The two tile shapes as separate kernels: the pair kernel carries its cluster shape in
+// its attributes, so it can be neither launched nor sized (occupancy) without it.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    ns_tc_pair_kernel(const __grid_constant__ NsParams p) {
+  ns_tc_body<true>(p);
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    ns_tc_single_kernel(const __grid_constant__ NsParams p) {
+  ns_tc_body<false>(p);
+}
+
 __global__ void selftest_timeout_kernel(int* err, long long budget) {
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
@@ -674,13 +686,13 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, ns_tc_kernel<kPair>, p);
+  e = cudaLaunchKernelEx(&cfg, kPair ? ns_tc_pair_kernel : ns_tc_single_kernel, p);
   if (e != cudaSuccess && kPair) {
     // Cluster kernels may not take the cooperative attribute; the grid is sized to the
     // device's resident-cluster count, so on an otherwise idle GPU all pairs are resident.
     (void)cudaGetLastError();
     cfg.numAttrs = 0;
-    e = cudaLaunchKernelEx(&cfg, ns_tc_kernel<kPair>, p);
+    e = cudaLaunchKernelEx(&cfg, kPair ? ns_tc_pair_kernel : ns_tc_single_kernel, p);
   }
   return e;
 }
@@ -689,7 +701,7 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
 
 cudaError_t prepare_ns_kernels(int* max_pairs, int* max_singles) {
   for (int k = 0; k < 2; ++k) {
-    const void* fn = k == 0 ? (const void*)ns_tc_kernel<false> : (const void*)ns_tc_kernel<true>;
+    const void* fn = k == 0 ? (const void*)ns_tc_single_kernel : (const void*)ns_tc_pair_kernel;
     const int smem = k == 0 ? Cfg<false>::SMEM_BYTES : Cfg<true>::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -699,7 +711,7 @@ cudaError_t prepare_ns_kernels(int* max_pairs, int* max_singles) {
   }
   int per_sm = 0, sms = 0, dev = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, ns_tc_kernel<false>, NUM_THREADS, Cfg<false>::SMEM_BYTES);
+      &per_sm, ns_tc_single_kernel, NUM_THREADS, Cfg<false>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -709,7 +721,7 @@ cudaError_t prepare_ns_kernels(int* max_pairs, int* max_singles) {
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = Cfg<true>::SMEM_BYTES;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, ns_tc_kernel<true>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, ns_tc_pair_kernel, &cfg);
   if (e != cudaSuccess) return e;
   *max_pairs = n;
   return cudaSuccess;
