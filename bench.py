@@ -64,9 +64,9 @@ def elementwise_bytes(n_matrix_elems, ns_dtype):
 # ns_tc_kernels_llama3_8b_x2.md).  Valid only for the kernel shape and the sources it was
 # taken with.
 NS_TRAFFIC = {
-    "llama3_8b_x32": {"bytes_per_launch": 16 * (21402986496 + 9351046912) / 15,
-                      "cta_pair": False,
-                      "sources_sha256": "c38ac66a52445128f7dd0ff5b37e9089e869439dfb4374ab63f6dfcd4d01472f"},
+    "llama3_8b_x32": {"bytes_per_launch": 16 * (22691102464 + 9351844352) / 15,
+                      "tile_shape": 3,
+                      "sources_sha256": "61bc5c421b99415a546b173525885f8f768b760904e90c0fac8a958b7168c593"},
 }
 NS_SOURCES = ("gemm_ns.cu", "device_common.cuh", "layout.cpp")
 
@@ -87,7 +87,7 @@ def ns_traffic(workload, ns_dtype, kernel):
     rec = NS_TRAFFIC.get(workload)
     if rec is None or ns_dtype != "bf16" or kernel is None:
         return None
-    if kernel["cta_pair"] != rec["cta_pair"]:
+    if kernel["tile_shape"] != rec["tile_shape"]:
         return None
     try:
         if _ns_sources_sha256() != rec["sources_sha256"]:
@@ -97,14 +97,19 @@ def ns_traffic(workload, ns_dtype, kernel):
     return rec["bytes_per_launch"]
 
 
+NS_KERNEL_NAMES = {
+    1: "ns_tc_single_kernel (tcgen05 cta_group::1, 128x256 tiles)",
+    2: "ns_tc_pair_kernel (tcgen05 cta_group::2, 256x256 tiles)",
+    3: "ns_tc_mcast_kernel (2-CTA clusters, cta_group::1 per CTA, multicast B, 256x256 tiles)",
+}
+
+
 def ns_kernel_label(kernel, ns_steps):
     if kernel is None:
         return "ns_phase_f32_kernel (fp32 CUDA cores, 3 launches per iteration)"
-    name = "ns_tc_pair_kernel (tcgen05 cta_group::2, 256x256 tiles)" if kernel["cta_pair"] \
-        else "ns_tc_single_kernel (tcgen05 cta_group::1, 128x256 tiles)"
     launches = 1 if kernel["persistent"] else 3 * ns_steps
     return "%s, %d units, %d launch(es) per step; the last Update also applies W" % (
-        name, kernel["units"], launches)
+        NS_KERNEL_NAMES[kernel["tile_shape"]], kernel["units"], launches)
 
 
 def load_peaks():

@@ -240,12 +240,14 @@ int32_t muon_abi_version(void);
 /* Which Newton-Schulz kernel `layout` runs on the current device; prepares the layout's
  * device tables there first if no call has (as the first step would).  The pages have no
  * counterpart: it reports a choice this library makes, for tests and measurements.
- * *cta_pair = 1: 2-CTA clusters computing 256 x 256 tiles (tcgen05 cta_group::2); 0: single
- * CTAs computing 128 x 256 tiles.  *units: CTAs (or CTA pairs) per launch.  *persistent = 1:
- * all phases of all iterations in one launch; 0: one launch per phase.  All three are 0 on
- * fp32 layouts and layouts without matrices.  MUON_ERR_UNSUPPORTED if the device is not
- * sm_103, or the environment pins a shape the device cannot run. */
-muon_status muon_layout_ns_kernel(const muon_layout* layout, int32_t* cta_pair, int32_t* units,
+ * *tile_shape: 1 = one CTA per 128 x 256 tile (tcgen05 cta_group::1); 2 = a 2-CTA cluster
+ * per 256 x 256 tile (cta_group::2); 3 = a 2-CTA cluster per 256 x 256 tile, each CTA
+ * computing its 128 rows with cta_group::1 and the shared operand multicast to both.
+ * *units: CTAs (shape 1) or clusters per launch.  *persistent = 1: all phases of all
+ * iterations in one launch; 0: one launch per phase.  All three are 0 on fp32 layouts and
+ * layouts without matrices.  MUON_ERR_UNSUPPORTED if the device is not sm_103, or the
+ * environment (MUON_TC_KERNEL) pins a shape the device cannot run. */
+muon_status muon_layout_ns_kernel(const muon_layout* layout, int32_t* tile_shape, int32_t* units,
                                   int32_t* persistent);
 /* Self-test of the bounded-wait path: launches one block that waits on an mbarrier nobody
  * arrives on, with a budget of budget_cycles clock cycles (1..2^40).  The wait runs out,

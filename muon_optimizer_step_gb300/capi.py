@@ -323,11 +323,12 @@ def muon_selftest_wait_timeout(budget_cycles, stream=None):
 
 def muon_layout_ns_kernel(layout) -> dict:
     """The Newton-Schulz kernel `layout` runs on the current device:
-    {"cta_pair": bool, "units": int, "persistent": bool}."""
-    pair, units, pers = _I32(), _I32(), _I32()
-    _check(lib.muon_layout_ns_kernel(layout.handle, ctypes.byref(pair), ctypes.byref(units),
+    {"tile_shape": 1 single CTA | 2 CTA pair | 3 cluster with multicast B (0: none),
+     "units": int, "persistent": bool}."""
+    shape, units, pers = _I32(), _I32(), _I32()
+    _check(lib.muon_layout_ns_kernel(layout.handle, ctypes.byref(shape), ctypes.byref(units),
                                      ctypes.byref(pers)), "muon_layout_ns_kernel")
-    return {"cta_pair": bool(pair.value), "units": int(units.value),
+    return {"tile_shape": int(shape.value), "units": int(units.value),
             "persistent": bool(pers.value)}
 
 

@@ -137,30 +137,33 @@ muon_status ensure_device(muon_layout* L) {
       free_tables(&t);
       return fail(MUON_ERR_UNSUPPORTED, "the tcgen05 kernel does not fit on an SM of device %d", dev);
     }
-    // CTA pairs (256 x 256 tiles) keep the tensor pipe busier per clock (74-76% of active
-    // cycles against 71% for single CTAs on two Llama-3-8B layers) and are 3-6% faster on
-    // the GPT-2, MoE and two-layer sets.  They also draw more power per clock, so a buffer
-    // whose steps run long enough to hold the GPU at its power limit runs single CTAs
-    // (128 x 256 tiles) at ~6% higher clocks: 1.3% faster on the Llama-3-8B set at 1.4 kW.
-    // The cut is the Newton-Schulz work of one iteration: 94 TFLOP on that set, 6 on the
-    // two-layer one.
+    // Three tile shapes, measured on GB300 (bench, bf16):
+    //  - CTA pairs (cta_group::2, 256 x 256 tiles) keep the tensor pipe busiest per clock
+    //    (74-76% of active cycles against 71% for single CTAs on two Llama-3-8B layers) and
+    //    are 2-6% faster wherever the clock stays high: GPT-2, MoE, two Llama layers.
+    //  - Steps long enough to hold the GPU at its 1.4 kW limit (the 32-layer Llama-3-8B
+    //    set) are decided by energy per flop instead.  There 2-CTA clusters that multicast
+    //    the shared B operand (each CTA on cta_group::1) clock highest (~1800 MHz against
+    //    ~1740 single, ~1600 pairs) and finish first: 356 ms against 359 and 361.
+    // The cut between the two regimes is the Newton-Schulz work of one iteration: 94 TFLOP
+    // on the 32-layer set, 6 on the two-layer one.
     double all = 0.0;  // flops of one iteration, symmetric count: 3 m^2 n + m^3 per matrix
     for (const MatDev& m : L->plan.mats)
       all += 3.0 * m.m * (double)m.m * m.n + (double)m.m * m.m * m.m;
-    bool pair = pairs >= 1 && all < 20e12;
-    const char* v = std::getenv("MUON_TC_KERNEL");  // "1" / "2" pins a shape (measurements)
-    if (v != nullptr && v[0] == '1') pair = false;
-    if (v != nullptr && v[0] == '2') {
-      if (pairs < 1) {
+    int shape = pairs < 1 ? kShapeSingle : (all < 20e12 ? kShapePair : kShapeMcast);
+    const char* v = std::getenv("MUON_TC_KERNEL");  // "1" / "2" / "3" pins a shape
+    if (v != nullptr && v[0] >= '1' && v[0] <= '3') {
+      shape = v[0] - '0';
+      if (shape != kShapeSingle && pairs < 1) {
         free_tables(&t);
         return fail(MUON_ERR_UNSUPPORTED,
-                    "MUON_TC_KERNEL=2 asks for CTA pairs, but no 2-CTA cluster of the tcgen05 "
-                    "kernel fits on device %d", dev);
+                    "MUON_TC_KERNEL=%d asks for 2-CTA clusters, but none of the tcgen05 "
+                    "kernel fits on device %d", shape, dev);
       }
-      pair = true;
     }
-    t.tc_pair = pair;
-    t.tc_units = pair ? pairs : singles;
+    const bool cluster = shape != kShapeSingle;
+    t.tc_shape = shape;
+    t.tc_units = cluster ? pairs : singles;
     // One persistent launch when a phase carries little work (< 100 GFLOP, e.g. the
     // GPT-2-small set: 8% faster there); a launch per phase otherwise (Llama-3-8B: twice as
     // fast as persistent; MoE: 16% faster), where each phase's tiles are balanced alone.
@@ -169,12 +172,12 @@ muon_status ensure_device(muon_layout* L) {
     if (pv != nullptr && (pv[0] == '0' || pv[0] == '1')) t.tc_persistent = pv[0] == '1';
     for (MatDev& m : L->plan.mats) m.sig[0] = m.sig[1] = m.sig[2] = 0;
     for (int p = 0; p < 3; ++p) {
-      TileList tl = pair ? plan_tiles(L->plan, p, 256, 256, kTcBK, t.tc_units, !t.tc_persistent)
+      TileList tl = cluster ? plan_tiles(L->plan, p, 256, 256, kTcBK, t.tc_units, !t.tc_persistent)
                          : plan_tiles(L->plan, p, kTcBM, kTcBN, kTcBK, t.tc_units,
                                       !t.tc_persistent);
       // Every unit of the persistent launch reads begin[unit + 1]: pad the offsets.
       while ((int)tl.cta_begin.size() < t.tc_units + 1) tl.cta_begin.push_back(tl.cta_begin.back());
-      for (const TileDev& td : tl.tiles) L->plan.mats[td.mat].sig[p] += pair ? 2 : 1;
+      for (const TileDev& td : tl.tiles) L->plan.mats[td.mat].sig[p] += cluster ? 2 : 1;
       t.grid[p] = tl.grid;
       if ((s = upload(tl.tiles, &t.tiles[p])) != MUON_OK) { free_tables(&t); return s; }
       if ((s = upload(tl.cta_begin, &t.cta_begin[p])) != MUON_OK) { free_tables(&t); return s; }
@@ -636,15 +639,15 @@ muon_status muon_check(cudaStream_t stream) {
   return ok();
 }
 
-muon_status muon_layout_ns_kernel(const muon_layout* layout, int32_t* cta_pair, int32_t* units,
+muon_status muon_layout_ns_kernel(const muon_layout* layout, int32_t* tile_shape, int32_t* units,
                                   int32_t* persistent) {
-  if (layout == nullptr || cta_pair == nullptr || units == nullptr || persistent == nullptr)
+  if (layout == nullptr || tile_shape == nullptr || units == nullptr || persistent == nullptr)
     return fail(MUON_ERR_INVALID_ARG, "null argument");
   muon_layout* L = const_cast<muon_layout*>(layout);
   std::lock_guard<std::mutex> guard(L->mu);
   MUON_TRY(ensure_device(L));
   const bool tc = L->plan.ns_dtype == MUON_NS_BF16 && !L->plan.mats.empty();
-  *cta_pair = tc && L->dt.tc_pair ? 1 : 0;
+  *tile_shape = tc ? L->dt.tc_shape : 0;
   *units = tc ? L->dt.tc_units : 0;
   *persistent = tc && L->dt.tc_persistent ? 1 : 0;
   return ok();

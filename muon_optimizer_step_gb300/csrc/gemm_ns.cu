@@ -53,21 +53,26 @@ constexpr int TMEM_COLS = 512;      // two 128 x 256 fp32 accumulators
 constexpr int MN_BOX_BYTES = 64 * BK * 2;
 constexpr float kA = 3.4445f, kB = -4.7750f, kC = 2.0315f;
 
-template <bool kPair>
+template <int kShape>
 struct Cfg {
-  static constexpr int BM = kPair ? 256 : 128;      // output rows per tile
-  static constexpr int BROWS = kPair ? 128 : 256;   // B-operand rows this CTA loads
-  static constexpr int A_BYTES = 128 * BK * 2;      // 16 KB
-  static constexpr int B_BYTES = BROWS * BK * 2;    // 16 KB (pair) / 32 KB (single)
+  static constexpr bool kCluster = kShape != kShapeSingle;  // a 2-CTA cluster per tile
+  static constexpr bool kTwoSm = kShape == kShapePair;      // tcgen05 cta_group::2
+  static constexpr int BM = kCluster ? 256 : 128;     // output rows per tile
+  static constexpr int MMA_M = kTwoSm ? 256 : 128;    // rows of one MMA instruction
+  static constexpr int BROWS = kCluster ? 128 : 256;  // B-operand rows this CTA loads
+  static constexpr int A_BYTES = 128 * BK * 2;        // 16 KB
+  // B rows held in this CTA's stage: its own half (pair), or all 256 (single; multicast,
+  // where the peer CTA's half arrives by multicast)
+  static constexpr int B_BYTES = (kTwoSm ? 128 : 256) * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = kPair ? 6 : 4;
+  static constexpr int STAGES = kTwoSm ? 6 : 4;
   // operand stages, 4 KB of epilogue staging per epilogue warp, alignment, barriers
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * 4096 + 1024 + 256;
 };
 
 struct NsParams {
   const TileDev* tiles[3];
-  const int32_t* begin[3];   // per phase: tile-list offsets per CTA (per pair for kPair)
+  const int32_t* begin[3];   // per phase: tile-list offsets per CTA (per cluster)
   const MatDev* mats;
   const CUtensorMap* tmaps;
   uint8_t* ws;
@@ -87,19 +92,19 @@ struct TileOps {
   int a_mn, b_mn;
 };
 
-template <bool kPair>
+template <bool kCluster>
 __device__ __forceinline__ TileOps tile_ops(const MatDev& mt, int phase, int x_in) {
   const int xk = x_in ? kMapX1K128 : kMapX0K128;
-  const int xkb = kPair ? xk : (x_in ? kMapX1K256 : kMapX0K256);
+  const int xkb = kCluster ? xk : (x_in ? kMapX1K256 : kMapX0K256);
   const int xmn = x_in ? kMapX1MN : kMapX0MN;
   TileOps o;
   if (phase == kPhaseGram) {
     if (mt.tall) { o.a_map = xmn; o.b_map = xmn; o.a_mn = 1; o.b_mn = 1; }
     else { o.a_map = xk; o.b_map = xkb; o.a_mn = 0; o.b_mn = 0; }
   } else if (phase == kPhasePoly) {
-    o.a_map = kMapAK128; o.b_map = kPair ? kMapAK128 : kMapAK256; o.a_mn = 0; o.b_mn = 0;
+    o.a_map = kMapAK128; o.b_map = kCluster ? kMapAK128 : kMapAK256; o.a_mn = 0; o.b_mn = 0;
   } else {
-    if (mt.tall) { o.a_map = xk; o.b_map = kPair ? kMapBK128 : kMapBK256; o.a_mn = 0; o.b_mn = 0; }
+    if (mt.tall) { o.a_map = xk; o.b_map = kCluster ? kMapBK128 : kMapBK256; o.a_mn = 0; o.b_mn = 0; }
     else { o.a_map = kMapBK128; o.b_map = xmn; o.a_mn = 0; o.b_mn = 1; }
   }
   return o;
@@ -297,11 +302,11 @@ __device__ __forceinline__ void epilogue_block(const NsParams& p, const MatDev& 
 }
 
 // Bounded wait; on expiry also tells the peer CTA of a pair to stop.
-template <bool kPair>
+template <bool kCluster>
 __device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, const NsParams& p,
                                           volatile int* abort, uint32_t peer_abort) {
   if (mbar_wait_bounded(bar, parity, p.budget, p.err, abort)) return true;
-  if (kPair) asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1) : "memory");
+  if (kCluster) asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1) : "memory");
   return false;
 }
 
@@ -332,9 +337,11 @@ __device__ __forceinline__ bool epi_any(bool v) {
   return r != 0;
 }
 
-template <bool kPair>
+template <int kShape>
 __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
-  using C = Cfg<kPair>;
+  using C = Cfg<kShape>;
+  constexpr bool kCluster = C::kCluster;
+  constexpr bool kTwoSm = C::kTwoSm;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -349,25 +356,28 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0: the CTA that issues MMAs
-  const int unit = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const uint32_t peer_abort = kPair ? mapa_shared(smem_u32(&abort_flag), rank ^ 1u) : 0u;
+  const uint32_t rank = kCluster ? cluster_ctarank() : 0u;  // pair: 0 issues the MMAs
+  const int unit = kCluster ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const uint32_t peer_abort = kCluster ? mapa_shared(smem_u32(&abort_flag), rank ^ 1u) : 0u;
+  // This CTA issues MMAs (all but the odd CTA of a cta_group::2 pair).
+  const bool mma_cta = !kTwoSm || rank == 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);   // the (even) CTA's arrival with the expected bytes
-      mbar_init(&empty[s], 1);  // the MMA commit
+      mbar_init(&full[s], 1);   // the (pair: even) CTA's arrival with the expected bytes
+      // the MMA commit; with multicast B, both CTAs' commits (the peer's copies land here)
+      mbar_init(&empty[s], kShape == kShapeMcast ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], (kPair ? 2 : 1) * EPI_WARPS);
+      mbar_init(&acc_empty[b], (kTwoSm ? 2 : 1) * EPI_WARPS);
     }
     mbar_init(mma_done, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 2) {
-    if (kPair) {
+    if (kTwoSm) {
       tmem_alloc_pair(tmem_slot, TMEM_COLS);
       tmem_relinquish_pair();
     } else {
@@ -376,7 +386,7 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
     }
   }
   tc_fence_before();
-  if (kPair) cluster_sync(); else __syncthreads();
+  if (kCluster) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   volatile int* abort = &abort_flag;
@@ -402,25 +412,25 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
             // One phase per launch: stream order already made the inputs complete.
             if (!chained) target = 0;
             if (!wait_counter(p.counters + slot, target, p.budget, p.err, abort)) {
-              if (kPair)
+              if (kCluster)
                 asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1) : "memory");
               ok = false;
               break;
             }
-            const TileOps ops = tile_ops<kPair>(mt, phase, x_in);
+            const TileOps ops = tile_ops<kCluster>(mt, phase, x_in);
             const CUtensorMap* amap = p.tmaps + (size_t)tile.mat * kMapsPerMat + ops.a_map;
             const CUtensorMap* bmap = p.tmaps + (size_t)tile.mat * kMapsPerMat + ops.b_map;
-            const int ia = tile.i0 + (kPair ? 128 * (int)rank : 0);
-            const int jr = tile.j0 + (kPair ? 128 * (int)rank : 0);
+            const int ia = tile.i0 + (kCluster ? 128 * (int)rank : 0);
+            const int jr = tile.j0 + (kCluster ? 128 * (int)rank : 0);
             for (int kb = 0; kb < tile.kblocks; ++kb) {
-              if (!wait_role<kPair>(&empty[stage], ph ^ 1u, p, abort, peer_abort)) {
+              if (!wait_role<kCluster>(&empty[stage], ph ^ 1u, p, abort, peer_abort)) {
                 ok = false;
                 break;
               }
               uint8_t* sa = tiles_smem + stage * C::STAGE_BYTES;
               uint8_t* sb = sa + C::A_BYTES;
               const int k0 = kb * BK;
-              if (kPair) {
+              if (kTwoSm) {
                 // Only the even CTA arrives, announcing both CTAs' bytes; the odd CTA's
                 // copies may land first (the transaction count dips below zero, which
                 // mbarriers allow; the phase still needs the even CTA's arrival).
@@ -446,7 +456,20 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
                 } else {
                   tma_load_2d(sa, amap, k0, ia, &full[stage]);
                 }
-                if (ops.b_mn) {
+                if (kShape == kShapeMcast) {
+                  // This CTA's half of B goes to both CTAs' stages, at the half's offset;
+                  // each CTA's full barrier counts both halves.
+                  const uint32_t sbh = smem_u32(sb) + rank * (uint32_t)(C::B_BYTES / 2);
+                  const uint32_t fb = smem_u32(&full[stage]);
+                  if (ops.b_mn) {
+#pragma unroll
+                    for (int q = 0; q < C::BROWS / 64; ++q)
+                      tma_load_2d_mcast(sbh + q * MN_BOX_BYTES, bmap, jr + 64 * q, k0, fb,
+                                        (uint16_t)0x3);
+                  } else {
+                    tma_load_2d_mcast(sbh, bmap, k0, jr, fb, (uint16_t)0x3);
+                  }
+                } else if (ops.b_mn) {
 #pragma unroll
                   for (int q = 0; q < C::BROWS / 64; ++q)
                     tma_load_2d(sb + q * MN_BOX_BYTES, bmap, jr + 64 * q, k0, &full[stage]);
@@ -464,15 +487,16 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
         }
       }
       // Every copy issued must land before the block exits (already true unless aborted).
-      // For a pair the even CTA's full barriers count both CTAs' copies.
-      if (rank == 0)
+      // For a pair the even CTA's full barriers count both CTAs' copies; with multicast B
+      // each CTA's count the peer's copies into it.
+      if (mma_cta)
         for (long long k = nfill - 1; k >= 0 && k >= nfill - C::STAGES; --k)
           wait_drain(&full[k % C::STAGES], (uint32_t)((k / C::STAGES) & 1), p.budget, p.err);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0 && rank == 0) {
+    if (lane == 0 && mma_cta) {
       int stage = 0;
       uint32_t ph = 0;
       int lt = 0;
@@ -484,10 +508,10 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
           for (int ti = p.begin[phase][unit]; ti < p.begin[phase][unit + 1]; ++ti, ++lt) {
             const TileDev tile = p.tiles[phase][ti];
             const MatDev& mt = p.mats[tile.mat];
-            const TileOps ops = tile_ops<kPair>(mt, phase, it & 1);
-            const uint32_t idesc = idesc_bf16(C::BM, BN, ops.a_mn, ops.b_mn);
+            const TileOps ops = tile_ops<kCluster>(mt, phase, it & 1);
+            const uint32_t idesc = idesc_bf16(C::MMA_M, BN, ops.a_mn, ops.b_mn);
             const int ab = lt & 1;
-            if (!wait_role<kPair>(&acc_empty[ab], (uint32_t)(((lt >> 1) & 1) ^ 1), p, abort,
+            if (!wait_role<kCluster>(&acc_empty[ab], (uint32_t)(((lt >> 1) & 1) ^ 1), p, abort,
                                   peer_abort)) {
               ok = false;
               break;
@@ -495,7 +519,7 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
             tc_fence_after();
             const uint32_t d = tmem_base + (uint32_t)(ab * BN);
             for (int kb = 0; kb < tile.kblocks && ok; ++kb) {
-              if (!wait_role<kPair>(&full[stage], ph, p, abort, peer_abort)) {
+              if (!wait_role<kCluster>(&full[stage], ph, p, abort, peer_abort)) {
                 ok = false;
                 break;
               }
@@ -508,10 +532,11 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
                                              : smem_desc_sw128(sa + kk * 32, 16, 1024);
                 const uint64_t bd = ops.b_mn ? smem_desc_sw128(sb + kk * 2048, MN_BOX_BYTES, 1024)
                                              : smem_desc_sw128(sb + kk * 32, 16, 1024);
-                if (kPair) tc_mma_f16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                if (kTwoSm) tc_mma_f16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                 else tc_mma_f16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
               }
-              if (kPair) tc_commit_pair(&empty[stage], (uint16_t)0x3);
+              if (kTwoSm) tc_commit_pair(&empty[stage], (uint16_t)0x3);
+              else if (kShape == kShapeMcast) tc_commit_mcast(&empty[stage], (uint16_t)0x3);
               else tc_commit(&empty[stage]);
               if (++stage == C::STAGES) {
                 stage = 0;
@@ -519,13 +544,13 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
               }
             }
             if (!ok) break;
-            if (kPair) tc_commit_pair(&acc_full[ab], (uint16_t)0x3);
+            if (kTwoSm) tc_commit_pair(&acc_full[ab], (uint16_t)0x3);
             else tc_commit(&acc_full[ab]);
           }
         }
       }
       // Every MMA issued must complete before TMEM is released.
-      if (kPair) tc_commit_pair(mma_done, (uint16_t)0x1);
+      if (kTwoSm) tc_commit_pair(mma_done, (uint16_t)0x1);
       else tc_commit(mma_done);
       wait_drain(mma_done, 0, p.budget, p.err);
     }
@@ -564,7 +589,7 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
               const float inv = p.inv_norm[tile.mat];
               s = phase == kPhaseGram ? inv * inv : inv;
             }
-            const int r0 = tile.i0 + (kPair ? 128 * (int)rank : 0) + 32 * q;
+            const int r0 = tile.i0 + (kCluster ? 128 * (int)rank : 0) + 32 * q;
             const int i = r0 + lane;
             const int c_first = half * (BN / 64), c_last = (half + 1) * (BN / 64);
 #pragma unroll 1
@@ -583,7 +608,7 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
           tc_fence_before();
           __syncwarp();
           if (ok && lane == 0) {
-            if (!kPair || rank == 0) mbar_arrive(&acc_empty[ab]);
+            if (!kTwoSm || rank == 0) mbar_arrive(&acc_empty[ab]);
             else mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[ab]), 0));
           }
           if (chained) {
@@ -607,31 +632,44 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
         }
       }
     }
-    if (stop && kPair)
+    if (stop && kCluster)
       asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1) : "memory");
     // Shared memory must outlive every bulk store that reads it.
     if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
   tc_fence_before();
-  if (kPair) cluster_sync(); else __syncthreads();
+  if (kCluster) cluster_sync(); else __syncthreads();
   if (warp == 2) {
     tc_fence_after();
-    if (kPair) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    if (kTwoSm) tmem_dealloc_pair(tmem_base, TMEM_COLS);
     else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
-// The two tile shapes as separate kernels: the pair kernel carries its cluster shape in
-// its attributes, so it can be neither launched nor sized (occupancy) without it.
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    ns_tc_pair_kernel(const __grid_constant__ NsParams p) {
-  ns_tc_body<true>(p);
-}
-
+// The tile shapes as separate kernels: the cluster kernels carry their cluster shape in
+// their attributes, so they can be neither launched nor sized (occupancy) without it.
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     ns_tc_single_kernel(const __grid_constant__ NsParams p) {
-  ns_tc_body<false>(p);
+  ns_tc_body<kShapeSingle>(p);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    ns_tc_pair_kernel(const __grid_constant__ NsParams p) {
+  ns_tc_body<kShapePair>(p);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    ns_tc_mcast_kernel(const __grid_constant__ NsParams p) {
+  ns_tc_body<kShapeMcast>(p);
+}
+
+using NsKernel = void (*)(NsParams);
+
+template <int kShape>
+NsKernel ns_tc_kernel_of() {
+  return kShape == kShapeSingle ? ns_tc_single_kernel
+                                : (kShape == kShapePair ? ns_tc_pair_kernel : ns_tc_mcast_kernel);
 }
 
 __global__ void selftest_timeout_kernel(int* err, long long budget) {
@@ -647,7 +685,7 @@ __global__ void selftest_timeout_kernel(int* err, long long budget) {
   if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, budget, err, &abort_flag);
 }
 
-template <bool kPair>
+template <int kShape>
 cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_steps,
                         int q_begin, int q_end, long long budget, const ApplyArgs* ap,
                         cudaStream_t st) {
@@ -675,9 +713,10 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((kPair ? 2 : 1) * dt.tc_units), 1, 1);
+  constexpr bool kCluster = Cfg<kShape>::kCluster;
+  cfg.gridDim = dim3((unsigned)((kCluster ? 2 : 1) * dt.tc_units), 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<kPair>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = Cfg<kShape>::SMEM_BYTES;
   cfg.stream = st;
   // Cooperative: every CTA must be resident at once, because tiles wait on tiles of
   // other CTAs.  The grid never exceeds one CTA (pair) per SM (TPC).
@@ -686,13 +725,13 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kPair ? ns_tc_pair_kernel : ns_tc_single_kernel, p);
-  if (e != cudaSuccess && kPair) {
+  e = cudaLaunchKernelEx(&cfg, ns_tc_kernel_of<kShape>(), p);
+  if (e != cudaSuccess && kCluster) {
     // Cluster kernels may not take the cooperative attribute; the grid is sized to the
     // device's resident-cluster count, so on an otherwise idle GPU all pairs are resident.
     (void)cudaGetLastError();
     cfg.numAttrs = 0;
-    e = cudaLaunchKernelEx(&cfg, kPair ? ns_tc_pair_kernel : ns_tc_single_kernel, p);
+    e = cudaLaunchKernelEx(&cfg, ns_tc_kernel_of<kShape>(), p);
   }
   return e;
 }
@@ -700,9 +739,13 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
 }  // namespace
 
 cudaError_t prepare_ns_kernels(int* max_pairs, int* max_singles) {
-  for (int k = 0; k < 2; ++k) {
-    const void* fn = k == 0 ? (const void*)ns_tc_single_kernel : (const void*)ns_tc_pair_kernel;
-    const int smem = k == 0 ? Cfg<false>::SMEM_BYTES : Cfg<true>::SMEM_BYTES;
+  const void* fns[3] = {(const void*)ns_tc_single_kernel, (const void*)ns_tc_pair_kernel,
+                        (const void*)ns_tc_mcast_kernel};
+  const int smems[3] = {Cfg<kShapeSingle>::SMEM_BYTES, Cfg<kShapePair>::SMEM_BYTES,
+                        Cfg<kShapeMcast>::SMEM_BYTES};
+  for (int k = 0; k < 3; ++k) {
+    const void* fn = fns[k];
+    const int smem = smems[k];
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -711,19 +754,25 @@ cudaError_t prepare_ns_kernels(int* max_pairs, int* max_singles) {
   }
   int per_sm = 0, sms = 0, dev = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, ns_tc_single_kernel, NUM_THREADS, Cfg<false>::SMEM_BYTES);
+      &per_sm, ns_tc_single_kernel, NUM_THREADS, Cfg<kShapeSingle>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   *max_singles = per_sm * sms;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * 1024, 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<true>::SMEM_BYTES;
-  int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, ns_tc_pair_kernel, &cfg);
-  if (e != cudaSuccess) return e;
-  *max_pairs = n;
+  // Resident 2-CTA clusters: the smaller count of the two cluster kernels.
+  int n_min = 1 << 30;
+  for (int k = 1; k < 3; ++k) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 1024, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smems[k];
+    int n = 0;
+    e = k == 1 ? cudaOccupancyMaxActiveClusters(&n, ns_tc_pair_kernel, &cfg)
+               : cudaOccupancyMaxActiveClusters(&n, ns_tc_mcast_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    n_min = n < n_min ? n : n_min;
+  }
+  *max_pairs = n_min;
   return cudaSuccess;
 }
 
@@ -736,8 +785,11 @@ cudaError_t launch_ns_tc(const Plan& plan, const DevTables& dt, void* ws, int ns
   const int step = dt.tc_persistent ? nq : 1;
   for (int q0 = 0; q0 < nq; q0 += step) {
     const cudaError_t e =
-        dt.tc_pair ? launch_impl<true>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
-                   : launch_impl<false>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st);
+        dt.tc_shape == kShapePair
+            ? launch_impl<kShapePair>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
+        : dt.tc_shape == kShapeMcast
+            ? launch_impl<kShapeMcast>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
+            : launch_impl<kShapeSingle>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

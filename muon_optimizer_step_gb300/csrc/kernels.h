@@ -14,6 +14,13 @@ struct ShardPtrs;
 struct ApplyArgs;
 struct GroupParams;
 
+// Tile shapes of the tcgen05 Newton-Schulz kernels (the values MUON_TC_KERNEL pins and
+// muon_layout_ns_kernel reports).
+constexpr int kShapeSingle = 1;  // one CTA per 128 x 256 tile, tcgen05 cta_group::1
+constexpr int kShapePair = 2;    // 2-CTA cluster per 256 x 256 tile, tcgen05 cta_group::2
+constexpr int kShapeMcast = 3;   // 2-CTA cluster per 256 x 256 tile, each CTA cta_group::1
+                                 // on its 128 rows, the B operand multicast to both
+
 // Device-resident tables of a layout (uploaded once per device).
 struct DevTables {
   int device = -1;
@@ -25,7 +32,7 @@ struct DevTables {
   int32_t* cta_begin[3] = {nullptr, nullptr, nullptr};
   int grid[3] = {0, 0, 0};
   CUtensorMap* tmaps = nullptr; // kMapsPerMat per matrix (bf16 path)
-  bool tc_pair = true;          // bf16 path: CTA pairs (256x256 tiles) or single CTAs (128x256)
+  int tc_shape = kShapeSingle;  // bf16 path: tile shape (kShape*)
   bool tc_persistent = false;   // bf16 path: all phases in one launch (tiles in matrix order)
   int tc_units = 0;             // bf16 path: CTAs (or pairs) of each launch; every
                                 // phase's cta_begin has tc_units + 1 entries

@@ -346,11 +346,11 @@ def test_wait_timeout_is_reported_and_context_survives(capi):
     assert float(x.sum()) == 16.0
 
 
-@pytest.mark.parametrize("variant", ["1", "2"])
+@pytest.mark.parametrize("variant", ["1", "2", "3"])
 @pytest.mark.parametrize("persistent", ["0", "1"])
 def test_each_tcgen05_variant_vs_oracle(capi, variant, persistent, monkeypatch):
-    """Both tcgen05 tile shapes (single CTA 128x256 tiles, CTA pairs 256x256 tiles) and
-    both launch modes (one launch per phase; one persistent launch whose tiles wait on
+    """The three tcgen05 tile shapes (single CTA 128x256 tiles; 256x256 tiles on CTA pairs,
+    and on 2-CTA clusters with multicast B) and both launch modes (one launch per phase; one persistent launch whose tiles wait on
     per-matrix counters), pinned one at a time, on ragged shapes and on a matrix that
     spans several pair tiles."""
     monkeypatch.setenv("MUON_TC_KERNEL", variant)
@@ -359,7 +359,7 @@ def test_each_tcgen05_variant_vs_oracle(capi, variant, persistent, monkeypatch):
     wl = inputs.Workload("mixed", tuple(shapes), (True,) * len(shapes), 1, seed=9, rank=4)
     lay = capi.muon_layout_create(wl.shapes, 1, 0, wl.is_matrix)
     k = capi.muon_layout_ns_kernel(lay)
-    assert k["cta_pair"] == (variant == "2") and k["persistent"] == (persistent == "1"), k
+    assert k["tile_shape"] == int(variant) and k["persistent"] == (persistent == "1"), k
     assert k["units"] >= 1
     ws = capi.workspace_tensor(lay)
     X = recipe_inputs(wl, 3)
@@ -441,9 +441,10 @@ def test_smoke_entry_point(capi):
 
 
 def test_default_kernel_choice(capi, monkeypatch):
-    """CTA pairs with a launch per phase for two Llama-3-8B layers; single CTAs for the
-    32-layer set (94 TFLOP per iteration: long enough to run at the power limit); CTA
-    pairs in one persistent launch for the GPT-2-small set; nothing on the fp32 path."""
+    """CTA pairs with a launch per phase for two Llama-3-8B layers; 2-CTA clusters with
+    multicast B for the 32-layer set (94 TFLOP per iteration: long enough to run at the
+    power limit); CTA pairs in one persistent launch for the GPT-2-small set; nothing on
+    the fp32 path."""
     monkeypatch.delenv("MUON_TC_KERNEL", raising=False)
     monkeypatch.delenv("MUON_NS_PERSISTENT", raising=False)
 
@@ -452,15 +453,15 @@ def test_default_kernel_choice(capi, monkeypatch):
         return capi.muon_layout_ns_kernel(capi.muon_layout_create(wl.shapes, 1, dtype,
                                                                   wl.is_matrix))
     k = choice("llama3_8b_x2")
-    assert k["cta_pair"] and not k["persistent"] and k["units"] >= 1, k
+    assert k["tile_shape"] == 2 and not k["persistent"] and k["units"] >= 1, k
     k = choice("llama3_8b_x32")
-    assert not k["cta_pair"] and not k["persistent"] and k["units"] >= 1, k
+    assert k["tile_shape"] == 3 and not k["persistent"] and k["units"] >= 1, k
     k = choice("gpt2_small_x12")
-    assert k["cta_pair"] and k["persistent"] and k["units"] >= 1, k
-    assert choice("gpt2_small_x12", 1) == {"cta_pair": False, "units": 0, "persistent": False}
+    assert k["tile_shape"] == 2 and k["persistent"] and k["units"] >= 1, k
+    assert choice("gpt2_small_x12", 1) == {"tile_shape": 0, "units": 0, "persistent": False}
 
 
-@pytest.mark.parametrize("variant", ["1", "2"])
+@pytest.mark.parametrize("variant", ["1", "2", "3"])
 @pytest.mark.parametrize("persistent", ["0", "1"])
 def test_fused_tail_each_variant(capi, variant, persistent, monkeypatch):
     """muon_step (whose last Update applies W) against the three separate stages, for each
