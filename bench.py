@@ -1,6 +1,6 @@
 """Benchmark of one Muon optimizer step on synthetic data (prints ONE JSON line on rank 0).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--ns-dtype bf16|fp32]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--ns-dtype bf16|fp32|split]
     python bench.py --impl reference ...   # the fp64 CPU oracle on this host's cores
 
 A step is the whole hot path over one flat buffer: momentum + orthogonalization input +
@@ -52,9 +52,10 @@ def ns_flops(shapes, is_matrix, ns_steps):
 def elementwise_bytes(n_matrix_elems, ns_dtype):
     """Algorithmic HBM bytes of the two streaming passes per step.
 
-    Stage 1 reads G and M and writes M (12 B) and X (2 B bf16 / 4 B fp32); stage 3 reads W
-    and O (2 / 4 B) and writes W (8 B): 24 B per element on the bf16 path."""
-    x = 2 if ns_dtype == "bf16" else 4
+    Stage 1 reads G and M and writes M (12 B) and X (2 B bf16 / 4 B fp32 / 6 B as three
+    bf16 parts); stage 3 reads W and O (2 / 4 / 6 B) and writes W (8 B): 24 B per element
+    on the bf16 path."""
+    x = {"bf16": 2, "fp32": 4, "split": 6}[ns_dtype]
     return n_matrix_elems * (12 + x), n_matrix_elems * (8 + x)
 
 
@@ -104,12 +105,15 @@ NS_KERNEL_NAMES = {
 }
 
 
-def ns_kernel_label(kernel, ns_steps):
+def ns_kernel_label(kernel, ns_steps, ns_dtype="bf16"):
     if kernel is None:
         return "ns_phase_f32_kernel (fp32 CUDA cores, 3 launches per iteration)"
     launches = 1 if kernel["persistent"] else 3 * ns_steps
+    name = NS_KERNEL_NAMES[kernel["tile_shape"]] if ns_dtype == "bf16" else \
+        "ns_tc_split_kernel (tcgen05 cta_group::2, fp32 as 3 bf16 parts, 6 products, " \
+        "256x256 tiles)"
     return "%s, %d units, %d launch(es) per step; the last Update also applies W" % (
-        NS_KERNEL_NAMES[kernel["tile_shape"]], kernel["units"], launches)
+        name, kernel["units"], launches)
 
 
 def load_peaks():
@@ -323,10 +327,11 @@ def run_ours(args):
     dev = torch.device("cuda", local)
 
     wl = inputs.WORKLOADS[args.workload]
-    ns_dtype = capi.MUON_NS_BF16 if args.ns_dtype == "bf16" else capi.MUON_NS_FP32
+    ns_dtype = {"bf16": capi.MUON_NS_BF16, "fp32": capi.MUON_NS_FP32,
+                "split": capi.MUON_NS_SPLIT_FP32}[args.ns_dtype]
     ns_steps = wl.ns_steps
     lay = capi.muon_layout_create(wl.shapes, wl.n_shards, ns_dtype, wl.is_matrix)
-    ns_kernel = capi.muon_layout_ns_kernel(lay) if ns_dtype == capi.MUON_NS_BF16 else None
+    ns_kernel = capi.muon_layout_ns_kernel(lay) if ns_dtype != capi.MUON_NS_FP32 else None
     S, L, N = wl.n_shards, lay.shard_len, lay.numel
     # One allocation per buffer; shard s is a view of [s*L, (s+1)*L), the first N elements
     # are the unsharded flat buffer.
@@ -468,7 +473,7 @@ def run_ours(args):
     sym, dense = ns_flops(wl.shapes, wl.is_matrix, ns_steps)
     n_mat_elems = sum(r * c for (r, c), f in zip(wl.shapes, wl.is_matrix) if f)
     b1, b3 = elementwise_bytes(n_mat_elems, args.ns_dtype)
-    fused_tail = args.ns_dtype == "bf16" and ns_steps >= 1
+    fused_tail = args.ns_dtype != "fp32" and ns_steps >= 1
     ns_ms = stage_ms[1]
     ns_tflops = sym / (ns_ms * 1e-3) / 1e12
     ew_ms = stage_ms[0]
@@ -476,6 +481,11 @@ def run_ours(args):
     if args.ns_dtype == "bf16":
         peak_tc = peaks["bf16_tflops_sustained"]
         peak_note = "%s bf16 sustained (cuBLAS loop under the power cap)" % peaks["source"]
+    elif args.ns_dtype == "split":
+        # six bf16 MMAs per useful product
+        peak_tc = peaks["bf16_tflops_sustained"] / 6.0
+        peak_note = ("%s bf16 sustained / 6 (six bf16 products per useful one)"
+                     % peaks["source"])
     else:
         # fp32 FMA issue rate: 128 FP32 lanes per SM x 2 flops x SMs x max SM clock.
         props = torch.cuda.get_device_properties(dev)
@@ -492,8 +502,10 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": args.ns_dtype,
         "dtype_detail": "fp32 weights, momentum and update arithmetic; Newton-Schulz on "
-                        + ("bf16 tensor-core operands with fp32 accumulation"
-                           if args.ns_dtype == "bf16" else "fp32 CUDA cores"),
+                        + {"bf16": "bf16 tensor-core operands with fp32 accumulation",
+                           "fp32": "fp32 CUDA cores",
+                           "split": "tensor cores, fp32 operands split into three bf16 "
+                                    "parts, six bf16 products each, fp32 accumulation"}[args.ns_dtype],
         "data": "synthetic",
         "config": {"workload": wl.name, "matrices": wl.n_matrices, "elements": N,
                    "n_shards": wl.n_shards, "ns_steps": ns_steps, "ns_dtype": args.ns_dtype,
@@ -502,8 +514,8 @@ def run_ours(args):
         "ns_flops_sym": sym, "matrices_per_s": wl.n_matrices / (ms * 1e-3),
         "stage_ms": {"momentum_inputs": stage_ms[0], "orthogonalize_apply": stage_ms[1]},
         "fused_apply": fused_tail,
-        "roofline": {"bound": "tensor" if args.ns_dtype == "bf16" else "alu",
-                     "kernel": ns_kernel_label(ns_kernel, ns_steps),
+        "roofline": {"bound": "alu" if args.ns_dtype == "fp32" else "tensor",
+                     "kernel": ns_kernel_label(ns_kernel, ns_steps, args.ns_dtype),
                      "achieved": ns_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": ns_tflops / peak_tc,
                      "traffic": ns_traffic(wl.name, args.ns_dtype, ns_kernel),
@@ -532,7 +544,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--ns-dtype", choices=["bf16", "fp32"], default="bf16")
+    ap.add_argument("--ns-dtype", choices=["bf16", "fp32", "split"], default="bf16")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

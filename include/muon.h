@@ -61,7 +61,13 @@ typedef enum muon_status {
 
 typedef enum muon_ns_dtype {
   MUON_NS_BF16 = 0,  /* Newton-Schulz on tcgen05 tensor cores: bf16 operands, fp32 accumulate */
-  MUON_NS_FP32 = 1   /* Newton-Schulz in fp32 on the CUDA cores (the precision path)          */
+  MUON_NS_FP32 = 1,  /* Newton-Schulz in fp32 on the CUDA cores (the precision path)          */
+  /* fp32-accurate Newton-Schulz on the tensor cores: every fp32 operand x is kept as three
+   * bf16 parts h = bf16(x), m = bf16(x - h), l = bf16(x - h - m), and every product takes
+   * six tcgen05 kind::f16 MMAs (hh + hm + mh + hl + lh + mm) accumulated in fp32, within
+   * about 2^-26 of the exact product.  The workspace holds the three parts (6 bytes per
+   * element of X, A and B).  No counterpart on the pages: a faster form of MUON_NS_FP32. */
+  MUON_NS_SPLIT_FP32 = 2
 } muon_ns_dtype;
 
 typedef struct muon_layout muon_layout; /* opaque */

@@ -22,6 +22,7 @@ MUON_ERR_OOM = 5
 MUON_ERR_UNSUPPORTED = 6
 MUON_NS_BF16 = 0
 MUON_NS_FP32 = 1
+MUON_NS_SPLIT_FP32 = 2
 MUON_MAX_SHARDS = 128
 WORKSPACE_ALIGN = 1024
 
@@ -191,7 +192,7 @@ def muon_layout_create(shapes, n_shards=1, ns_dtype=MUON_NS_BF16, is_matrix=None
             raise ValueError("is_matrix must have one flag per shape")
         flags = (ctypes.c_uint8 * max(1, n))(*is_matrix)
     if isinstance(ns_dtype, str):
-        ns_dtype = {"bf16": MUON_NS_BF16, "fp32": MUON_NS_FP32}[ns_dtype]
+        ns_dtype = {"bf16": MUON_NS_BF16, "fp32": MUON_NS_FP32, "split": MUON_NS_SPLIT_FP32}[ns_dtype]
     h = ctypes.c_void_p()
     _check(lib.muon_layout_create(flat, flags, n, int(n_shards), int(ns_dtype), ctypes.byref(h)),
            "muon_layout_create")

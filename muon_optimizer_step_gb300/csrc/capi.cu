@@ -119,8 +119,9 @@ muon_status ensure_device(muon_layout* L) {
   muon_status s;
   if ((s = err_word(dev, &t.err)) != MUON_OK) return s;
   if ((s = upload(L->plan.chunks, &t.chunks)) != MUON_OK) { free_tables(&t); return s; }
-  const bool bf16 = L->plan.ns_dtype == MUON_NS_BF16;
-  if (!bf16) {
+  const bool tc = L->plan.ns_dtype != MUON_NS_FP32;  // a tcgen05 path (bf16 or split fp32)
+  const bool split = L->plan.ns_dtype == MUON_NS_SPLIT_FP32;
+  if (!tc) {
     for (int p = 0; p < 3; ++p) {
       const TileList tl = plan_tiles(L->plan, p, kF32BM, kF32BN, 16, sms);
       t.grid[p] = tl.grid;
@@ -151,7 +152,16 @@ muon_status ensure_device(muon_layout* L) {
     for (const MatDev& m : L->plan.mats)
       all += 3.0 * m.m * (double)m.m * m.n + (double)m.m * m.m * m.m;
     int shape = pairs < 1 ? kShapeSingle : (all < 20e12 ? kShapePair : kShapeMcast);
-    const char* v = std::getenv("MUON_TC_KERNEL");  // "1" / "2" / "3" pins a shape
+    const char* v = split ? nullptr : std::getenv("MUON_TC_KERNEL");  // "1"-"3" pins a shape
+    if (split) {
+      // The split-fp32 kernel exists for CTA pairs only (two 96 KB operand stages).
+      if (pairs < 1) {
+        free_tables(&t);
+        return fail(MUON_ERR_UNSUPPORTED,
+                    "the split-fp32 kernel needs 2-CTA clusters, and none fits on device %d", dev);
+      }
+      shape = kShapePair;
+    }
     if (v != nullptr && v[0] >= '1' && v[0] <= '3') {
       shape = v[0] - '0';
       if (shape != kShapeSingle && pairs < 1) {
@@ -167,14 +177,16 @@ muon_status ensure_device(muon_layout* L) {
     // One persistent launch when a phase carries little work (< 100 GFLOP, e.g. the
     // GPT-2-small set: 8% faster there); a launch per phase otherwise (Llama-3-8B: twice as
     // fast as persistent; MoE: 16% faster), where each phase's tiles are balanced alone.
-    t.tc_persistent = all / 3.0 < 100e9;
-    const char* pv = std::getenv("MUON_NS_PERSISTENT");  // "1" / "0" pins the launch mode
+    // The split-fp32 epilogue writes with plain stores, which the persistent launch's
+    // counters do not publish to the next phase's TMA reads: one launch per phase there.
+    t.tc_persistent = !split && all / 3.0 < 100e9;
+    const char* pv = split ? nullptr : std::getenv("MUON_NS_PERSISTENT");  // "1"/"0" pins it
     if (pv != nullptr && (pv[0] == '0' || pv[0] == '1')) t.tc_persistent = pv[0] == '1';
     for (MatDev& m : L->plan.mats) m.sig[0] = m.sig[1] = m.sig[2] = 0;
     for (int p = 0; p < 3; ++p) {
       TileList tl = cluster ? plan_tiles(L->plan, p, 256, 256, kTcBK, t.tc_units, !t.tc_persistent)
-                         : plan_tiles(L->plan, p, kTcBM, kTcBN, kTcBK, t.tc_units,
-                                      !t.tc_persistent);
+                            : plan_tiles(L->plan, p, kTcBM, kTcBN, kTcBK, t.tc_units,
+                                         !t.tc_persistent);
       // Every unit of the persistent launch reads begin[unit + 1]: pad the offsets.
       while ((int)tl.cta_begin.size() < t.tc_units + 1) tl.cta_begin.push_back(tl.cta_begin.back());
       for (const TileDev& td : tl.tiles) L->plan.mats[td.mat].sig[p] += cluster ? 2 : 1;
@@ -190,10 +202,10 @@ muon_status ensure_device(muon_layout* L) {
   return MUON_OK;
 }
 
-// Encodes the TMA descriptors for this workspace (bf16 path) when it changes.
+// Encodes the TMA descriptors for this workspace (tensor-core paths) when it changes.
 muon_status ensure_tmaps(muon_layout* L, const void* ws) {
   DevTables& dt = L->dt;
-  if (L->plan.ns_dtype != MUON_NS_BF16 || L->plan.mats.empty() || dt.tmap_ws == ws)
+  if (L->plan.ns_dtype == MUON_NS_FP32 || L->plan.mats.empty() || dt.tmap_ws == ws)
     return MUON_OK;
   std::vector<CUtensorMap> maps;
   std::string err;
@@ -278,7 +290,7 @@ muon_status run_momentum(muon_layout* L, const ShardPtrs& g, const ShardPtrs& m,
 }
 
 muon_status run_ns(muon_layout* L, void* ws, int ns_steps, const ApplyArgs* ap, cudaStream_t st) {
-  if (L->plan.ns_dtype == MUON_NS_BF16) {
+  if (L->plan.ns_dtype != MUON_NS_FP32) {
     MUON_CUDA(launch_ns_tc(L->plan, L->dt, ws, ns_steps, kDefaultBudget, ap, st), "newton_schulz");
     return MUON_OK;
   }
@@ -304,7 +316,7 @@ muon_status run_apply(muon_layout* L, const ShardPtrs& w, void* ws, const GroupP
 
 muon_status run_ns_apply(muon_layout* L, const ShardPtrs& w, void* ws, const GroupParams& gp,
                          int ns_steps, cudaStream_t st) {
-  if (L->plan.ns_dtype == MUON_NS_BF16 && ns_steps >= 1) {
+  if (L->plan.ns_dtype != MUON_NS_FP32 && ns_steps >= 1) {
     ApplyArgs ap;
     ap.W = w;
     ap.L = L->plan.L;
@@ -646,7 +658,7 @@ muon_status muon_layout_ns_kernel(const muon_layout* layout, int32_t* tile_shape
   muon_layout* L = const_cast<muon_layout*>(layout);
   std::lock_guard<std::mutex> guard(L->mu);
   MUON_TRY(ensure_device(L));
-  const bool tc = L->plan.ns_dtype == MUON_NS_BF16 && !L->plan.mats.empty();
+  const bool tc = L->plan.ns_dtype != MUON_NS_FP32 && !L->plan.mats.empty();
   *tile_shape = tc ? L->dt.tc_shape : 0;
   *units = tc ? L->dt.tc_units : 0;
   *persistent = tc && L->dt.tc_persistent ? 1 : 0;

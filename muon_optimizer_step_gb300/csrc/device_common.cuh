@@ -199,6 +199,26 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
          ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// ------------------------------------------------------------------ split fp32 (bf16 x 3)
+// An fp32 value x kept as three bf16 values h = bf16(x), m = bf16(x - h),
+// l = bf16(x - h - m) (each difference is exact in fp32), in three equal arrays: the m
+// and l arrays of a buffer follow its h array, each sized to whole kWsAlign units.
+// h + m + l recovers x to within 2^-26 |x|, and a product of two such values is
+// hh + hm + mh + hl + lh + mm up to about 2^-26 of it (the ml, lm, ll terms are dropped),
+// below the rounding of one fp32 product.
+struct Bf16x3 {};
+
+__host__ __device__ constexpr int64_t split_part_bytes(int64_t part_bytes) {
+  return (part_bytes + kWsAlign - 1) / kWsAlign * kWsAlign;
+}
+
+__device__ __forceinline__ void split_bf16x3(float x, __nv_bfloat16& h, __nv_bfloat16& m,
+                                             __nv_bfloat16& l) {
+  h = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(h);
+  m = __float2bfloat16_rn(r1);
+  l = __float2bfloat16_rn(r1 - __bfloat162float(m));
+}
 
 // ------------------------------------------------------------------ clusters / CTA pairs
 __device__ __forceinline__ uint32_t cluster_ctarank() {

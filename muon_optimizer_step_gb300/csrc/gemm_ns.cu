@@ -46,26 +46,32 @@ namespace {
 constexpr int NUM_THREADS = 384;  // 12 warps: producer, MMA issuer, TMEM allocator, idle, 8 epilogue
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
-constexpr int BK = kTcBK;           // 64 bf16 = one 128-byte swizzle row
 constexpr int BN = 256;             // output tile columns
-constexpr int UMMA_K = 16;
 constexpr int TMEM_COLS = 512;      // two 128 x 256 fp32 accumulators
-constexpr int MN_BOX_BYTES = 64 * BK * 2;
 constexpr float kA = 3.4445f, kB = -4.7750f, kC = 2.0315f;
 
-template <int kShape>
+// kSplit: the split-fp32 form (every fp32 operand kept as three bf16 parts h, m, l; six
+// kind::f16 MMAs per product: hh + hm + mh + hl + lh + mm); otherwise one bf16 operand.
+template <int kShape, bool kSplit = false>
 struct Cfg {
   static constexpr bool kCluster = kShape != kShapeSingle;  // a 2-CTA cluster per tile
   static constexpr bool kTwoSm = kShape == kShapePair;      // tcgen05 cta_group::2
-  static constexpr int BM = kCluster ? 256 : 128;     // output rows per tile
+  static constexpr int BK = 64;                       // k-block: one 128-byte row of bf16
+  static constexpr int UMMA_K = 16;                   // K of one MMA: 32 bytes of a row
+  static constexpr int PARTS = kSplit ? 3 : 1;        // operand copies: h (m, l)
+  static constexpr int MN_W = 64;                     // MN extent of an MN-major box
+  static constexpr int MN_BOX = BK * 128;             // bytes of an MN-major box (BK rows)
   static constexpr int MMA_M = kTwoSm ? 256 : 128;    // rows of one MMA instruction
   static constexpr int BROWS = kCluster ? 128 : 256;  // B-operand rows this CTA loads
-  static constexpr int A_BYTES = 128 * BK * 2;        // 16 KB
+  static constexpr int A_PART = 128 * 128;            // 16 KB: 128 rows of 128 bytes
   // B rows held in this CTA's stage: its own half (pair), or all 256 (single; multicast,
   // where the peer CTA's half arrives by multicast)
-  static constexpr int B_BYTES = (kTwoSm ? 128 : 256) * BK * 2;
+  static constexpr int B_PART = (kTwoSm ? 128 : 256) * 128;
+  static constexpr int A_BYTES = A_PART * PARTS;
+  static constexpr int B_BYTES = B_PART * PARTS;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = kTwoSm ? 6 : 4;
+  static constexpr int STAGES = kTwoSm ? (kSplit ? 2 : 6) : 4;
+  static_assert(!kSplit || kTwoSm, "the split-fp32 form runs on CTA pairs only");
   // operand stages, 4 KB of epilogue staging per epilogue warp, alignment, barriers
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * 4096 + 1024 + 256;
 };
@@ -301,6 +307,127 @@ __device__ __forceinline__ void epilogue_block(const NsParams& p, const MatDev& 
   st.pending = true;
 }
 
+// ---------------------------------------------------------------- split-fp32 epilogue
+// Row run of 32 split values at element index e of a buffer whose m and l arrays are
+// `part` elements after its h array: loads h + (m + l), or stores the split of f.
+// n < 32 takes the first n only.
+__device__ __forceinline__ void load_split_run(const __nv_bfloat16* h, int64_t part, int64_t e,
+                                               int n, float (&x)[32]) {
+  if (n == 32) {
+    uint4 u[3][4];
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) u[k][q] = *reinterpret_cast<const uint4*>(h + k * part + e + 8 * q);
+    float hf[32], mf[32], lf[32];
+    unpack_bf16x32(u[0], hf);
+    unpack_bf16x32(u[1], mf);
+    unpack_bf16x32(u[2], lf);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) x[t] = hf[t] + (mf[t] + lf[t]);
+  } else {
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+      x[t] = t < n ? __bfloat162float(h[e + t]) + (__bfloat162float(h[part + e + t]) +
+                                                   __bfloat162float(h[2 * part + e + t]))
+                   : 0.f;
+  }
+}
+
+__device__ __forceinline__ void store_split1(__nv_bfloat16* h, int64_t part, int64_t e, float f) {
+  __nv_bfloat16 hb, mb, lb;
+  split_bf16x3(f, hb, mb, lb);
+  h[e] = hb;
+  h[part + e] = mb;
+  h[2 * part + e] = lb;
+}
+
+__device__ __forceinline__ void store_split_run(__nv_bfloat16* h, int64_t part, int64_t e, int n,
+                                                const float (&f)[32]) {
+  if (n == 32) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t w[3][4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        __nv_bfloat16 h0, m0, l0, h1, m1, l1;
+        split_bf16x3(f[8 * q + 2 * k], h0, m0, l0);
+        split_bf16x3(f[8 * q + 2 * k + 1], h1, m1, l1);
+        w[0][k] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        w[1][k] = (uint32_t)__bfloat16_as_ushort(m0) | ((uint32_t)__bfloat16_as_ushort(m1) << 16);
+        w[2][k] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+      }
+#pragma unroll
+      for (int k = 0; k < 3; ++k)
+        *reinterpret_cast<uint4*>(h + k * part + e + 8 * q) = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
+    }
+  } else {
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+      if (t < n) store_split1(h, part, e + t, f[t]);
+  }
+}
+
+// Epilogue of a 32 x 32 block on the split-fp32 path: the same arithmetic as
+// epilogue_block on fp32 values (inputs h + m + l), written back as three bf16 parts with
+// plain stores: the row run of each lane, and for symmetric outputs the transposed block,
+// whose stores are coalesced across the warp (lane = column of the mirror row).  Diagonal
+// blocks keep the element rule (j >= i written, j > i mirrored).
+__device__ __forceinline__ void epilogue_block_split(const NsParams& p, const MatDev& mt,
+                                                     int phase, int x_in, bool apply, int r0,
+                                                     int jb, int lane, const uint32_t (&acc)[32],
+                                                     float s) {
+  const int i = r0 + lane;
+  float f[32];
+  if (phase == kPhaseUpdate) {
+    if (r0 >= mt.rows || jb >= mt.cols) return;  // warp-uniform
+    const int64_t part = split_part_bytes((int64_t)mt.rows * mt.ldx * 2) / 2;
+    const __nv_bfloat16* xin = reinterpret_cast<const __nv_bfloat16*>(p.ws + (x_in ? mt.x1 : mt.x0));
+    __nv_bfloat16* xout = reinterpret_cast<__nv_bfloat16*>(p.ws + (x_in ? mt.x0 : mt.x1));
+    const int n = i < mt.rows ? min(32, mt.cols - jb) : 0;
+    const int64_t e = (int64_t)i * mt.ldx + jb;
+    float x[32];
+    load_split_run(xin, part, e, n, x);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) f[t] = s * fmaf(kA, x[t], __uint_as_float(acc[t]));
+    if (apply && n > 0) apply_row_run(p.ap, mt, i, jb, n, f);
+    if (n > 0) store_split_run(xout, part, e, n, f);
+    return;
+  }
+  if (r0 >= mt.m || jb >= mt.m || jb < r0) return;  // outside, or below the diagonal
+  const int64_t part = split_part_bytes((int64_t)mt.m * mt.lda * 2) / 2;
+  __nv_bfloat16* am = reinterpret_cast<__nv_bfloat16*>(p.ws + mt.a);
+  const int n = i < mt.m ? min(32, mt.m - jb) : 0;
+  const int64_t e = (int64_t)i * mt.lda + jb;
+  if (phase == kPhaseGram) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) f[t] = __uint_as_float(acc[t]) * s;
+  } else {
+    float a[32];
+    load_split_run(am, part, e, n, a);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) f[t] = fmaf(kB, a[t], kC * __uint_as_float(acc[t]));
+  }
+  __nv_bfloat16* out = phase == kPhaseGram ? am : reinterpret_cast<__nv_bfloat16*>(p.ws + mt.b);
+  if (jb == r0) {
+    if (i < mt.m) {
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        const int j = jb + t;
+        if (j >= i && j < mt.m) store_split1(out, part, (int64_t)i * mt.lda + j, f[t]);
+        if (j > i && j < mt.m) store_split1(out, part, (int64_t)j * mt.lda + i, f[t]);
+      }
+    }
+    return;
+  }
+  if (n > 0) store_split_run(out, part, e, n, f);
+  if (i < mt.m) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+      if (jb + t < mt.m) store_split1(out, part, (int64_t)(jb + t) * mt.lda + i, f[t]);
+  }
+}
+
 // Bounded wait; on expiry also tells the peer CTA of a pair to stop.
 template <bool kCluster>
 __device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, const NsParams& p,
@@ -337,9 +464,9 @@ __device__ __forceinline__ bool epi_any(bool v) {
   return r != 0;
 }
 
-template <int kShape>
+template <int kShape, bool kSplit = false>
 __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
-  using C = Cfg<kShape>;
+  using C = Cfg<kShape, kSplit>;
   constexpr bool kCluster = C::kCluster;
   constexpr bool kTwoSm = C::kTwoSm;
   extern __shared__ uint8_t smem_raw[];
@@ -429,30 +556,39 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
               }
               uint8_t* sa = tiles_smem + stage * C::STAGE_BYTES;
               uint8_t* sb = sa + C::A_BYTES;
-              const int k0 = kb * BK;
+              const int k0 = kb * C::BK;
               if (kTwoSm) {
                 // Only the even CTA arrives, announcing both CTAs' bytes; the odd CTA's
                 // copies may land first (the transaction count dips below zero, which
                 // mbarriers allow; the phase still needs the even CTA's arrival).
                 if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
                 const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
-                if (ops.a_mn) {
-                  tma_load_2d_pair(smem_u32(sa), amap, ia, k0, fbar);
-                  tma_load_2d_pair(smem_u32(sa) + MN_BOX_BYTES, amap, ia + 64, k0, fbar);
-                } else {
-                  tma_load_2d_pair(smem_u32(sa), amap, k0, ia, fbar);
-                }
-                if (ops.b_mn) {
-                  tma_load_2d_pair(smem_u32(sb), bmap, jr, k0, fbar);
-                  tma_load_2d_pair(smem_u32(sb) + MN_BOX_BYTES, bmap, jr + 64, k0, fbar);
-                } else {
-                  tma_load_2d_pair(smem_u32(sb), bmap, k0, jr, fbar);
+#pragma unroll
+                for (int part = 0; part < C::PARTS; ++part) {  // h (then m, l: split fp32)
+                  const CUtensorMap* am = amap + part * kMapPart;
+                  const CUtensorMap* bm = bmap + part * kMapPart;
+                  const uint32_t da = smem_u32(sa) + part * C::A_PART;
+                  const uint32_t db = smem_u32(sb) + part * C::B_PART;
+                  if (ops.a_mn) {
+#pragma unroll
+                    for (int q = 0; q < 128 / C::MN_W; ++q)
+                      tma_load_2d_pair(da + q * C::MN_BOX, am, ia + q * C::MN_W, k0, fbar);
+                  } else {
+                    tma_load_2d_pair(da, am, k0, ia, fbar);
+                  }
+                  if (ops.b_mn) {
+#pragma unroll
+                    for (int q = 0; q < 128 / C::MN_W; ++q)
+                      tma_load_2d_pair(db + q * C::MN_BOX, bm, jr + q * C::MN_W, k0, fbar);
+                  } else {
+                    tma_load_2d_pair(db, bm, k0, jr, fbar);
+                  }
                 }
               } else {
                 mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
                 if (ops.a_mn) {
                   tma_load_2d(sa, amap, ia, k0, &full[stage]);
-                  tma_load_2d(sa + MN_BOX_BYTES, amap, ia + 64, k0, &full[stage]);
+                  tma_load_2d(sa + C::MN_BOX, amap, ia + C::MN_W, k0, &full[stage]);
                 } else {
                   tma_load_2d(sa, amap, k0, ia, &full[stage]);
                 }
@@ -463,16 +599,16 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
                   const uint32_t fb = smem_u32(&full[stage]);
                   if (ops.b_mn) {
 #pragma unroll
-                    for (int q = 0; q < C::BROWS / 64; ++q)
-                      tma_load_2d_mcast(sbh + q * MN_BOX_BYTES, bmap, jr + 64 * q, k0, fb,
+                    for (int q = 0; q < C::BROWS / C::MN_W; ++q)
+                      tma_load_2d_mcast(sbh + q * C::MN_BOX, bmap, jr + C::MN_W * q, k0, fb,
                                         (uint16_t)0x3);
                   } else {
                     tma_load_2d_mcast(sbh, bmap, k0, jr, fb, (uint16_t)0x3);
                   }
                 } else if (ops.b_mn) {
 #pragma unroll
-                  for (int q = 0; q < C::BROWS / 64; ++q)
-                    tma_load_2d(sb + q * MN_BOX_BYTES, bmap, jr + 64 * q, k0, &full[stage]);
+                  for (int q = 0; q < C::BROWS / C::MN_W; ++q)
+                    tma_load_2d(sb + q * C::MN_BOX, bmap, jr + C::MN_W * q, k0, &full[stage]);
                 } else {
                   tma_load_2d(sb, bmap, k0, jr, &full[stage]);
                 }
@@ -526,14 +662,35 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
               tc_fence_after();
               const uint32_t sa = sbase + stage * C::STAGE_BYTES;
               const uint32_t sb = sa + C::A_BYTES;
+              // One MMA reads 32 bytes of every operand row: +32 B along a K-major row, or
+              // UMMA_K rows of 128 B of an MN-major box.
+              constexpr uint32_t kMnStep = C::UMMA_K * 128;
 #pragma unroll
-              for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                const uint64_t ad = ops.a_mn ? smem_desc_sw128(sa + kk * 2048, MN_BOX_BYTES, 1024)
-                                             : smem_desc_sw128(sa + kk * 32, 16, 1024);
-                const uint64_t bd = ops.b_mn ? smem_desc_sw128(sb + kk * 2048, MN_BOX_BYTES, 1024)
-                                             : smem_desc_sw128(sb + kk * 32, 16, 1024);
-                if (kTwoSm) tc_mma_f16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-                else tc_mma_f16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
+                const uint32_t koff_a = ops.a_mn ? kk * kMnStep : kk * 32;
+                const uint32_t koff_b = ops.b_mn ? kk * kMnStep : kk * 32;
+                const uint32_t lbo_a = ops.a_mn ? C::MN_BOX : 16;
+                const uint32_t lbo_b = ops.b_mn ? C::MN_BOX : 16;
+                const uint64_t ad = smem_desc_sw128(sa + koff_a, lbo_a, 1024);
+                const uint64_t bd = smem_desc_sw128(sb + koff_b, lbo_b, 1024);
+                const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+                if (kSplit) {
+                  // x*y ~ hh + hm + mh + hl + lh + mm, all accumulated in fp32
+                  const uint64_t ad_m = smem_desc_sw128(sa + C::A_PART + koff_a, lbo_a, 1024);
+                  const uint64_t bd_m = smem_desc_sw128(sb + C::B_PART + koff_b, lbo_b, 1024);
+                  const uint64_t ad_l = smem_desc_sw128(sa + 2 * C::A_PART + koff_a, lbo_a, 1024);
+                  const uint64_t bd_l = smem_desc_sw128(sb + 2 * C::B_PART + koff_b, lbo_b, 1024);
+                  tc_mma_f16_pair(d, ad, bd, idesc, acc);
+                  tc_mma_f16_pair(d, ad, bd_m, idesc, 1u);
+                  tc_mma_f16_pair(d, ad_m, bd, idesc, 1u);
+                  tc_mma_f16_pair(d, ad, bd_l, idesc, 1u);
+                  tc_mma_f16_pair(d, ad_l, bd, idesc, 1u);
+                  tc_mma_f16_pair(d, ad_m, bd_m, idesc, 1u);
+                } else if (kTwoSm) {
+                  tc_mma_f16_pair(d, ad, bd, idesc, acc);
+                } else {
+                  tc_mma_f16(d, ad, bd, idesc, acc);
+                }
               }
               if (kTwoSm) tc_commit_pair(&empty[stage], (uint16_t)0x3);
               else if (kShape == kShapeMcast) tc_commit_mcast(&empty[stage], (uint16_t)0x3);
@@ -594,15 +751,22 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
             const int c_first = half * (BN / 64), c_last = (half + 1) * (BN / 64);
 #pragma unroll 1
             for (int c = c_first; c < c_last; ++c) {
-              uint4 in_cur[4];
-              const bool have_cur = epilogue_prefetch(p, mt, phase, x_in, i, tile.j0 + 32 * c,
-                                                      in_cur);
               uint32_t v[32];
-              tmem_ld_32x32b_x32(
-                  tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * BN + 32 * c), v);
-              tmem_ld_wait();
-              epilogue_block(p, mt, tile.mat, phase, x_in, apply, r0, tile.j0 + 32 * c, lane, v, s,
-                             in_cur, have_cur, est);
+              if constexpr (kSplit) {
+                tmem_ld_32x32b_x32(
+                    tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * BN + 32 * c), v);
+                tmem_ld_wait();
+                epilogue_block_split(p, mt, phase, x_in, apply, r0, tile.j0 + 32 * c, lane, v, s);
+              } else {
+                uint4 in_cur[4];
+                const bool have_cur = epilogue_prefetch(p, mt, phase, x_in, i, tile.j0 + 32 * c,
+                                                        in_cur);
+                tmem_ld_32x32b_x32(
+                    tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * BN + 32 * c), v);
+                tmem_ld_wait();
+                epilogue_block(p, mt, tile.mat, phase, x_in, apply, r0, tile.j0 + 32 * c, lane,
+                               v, s, in_cur, have_cur, est);
+              }
             }
           }
           tc_fence_before();
@@ -664,6 +828,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   ns_tc_body<kShapeMcast>(p);
 }
 
+// The split-fp32 form, on CTA pairs.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    ns_tc_split_kernel(const __grid_constant__ NsParams p) {
+  ns_tc_body<kShapePair, true>(p);
+}
+
 using NsKernel = void (*)(NsParams);
 
 template <int kShape>
@@ -685,7 +855,7 @@ __global__ void selftest_timeout_kernel(int* err, long long budget) {
   if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, budget, err, &abort_flag);
 }
 
-template <int kShape>
+template <int kShape, bool kSplit = false>
 cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_steps,
                         int q_begin, int q_end, long long budget, const ApplyArgs* ap,
                         cudaStream_t st) {
@@ -713,10 +883,11 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  constexpr bool kCluster = Cfg<kShape>::kCluster;
+  constexpr bool kCluster = Cfg<kShape, kSplit>::kCluster;
+  const NsKernel kernel = kSplit ? ns_tc_split_kernel : ns_tc_kernel_of<kShape>();
   cfg.gridDim = dim3((unsigned)((kCluster ? 2 : 1) * dt.tc_units), 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<kShape>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = Cfg<kShape, kSplit>::SMEM_BYTES;
   cfg.stream = st;
   // Cooperative: every CTA must be resident at once, because tiles wait on tiles of
   // other CTAs.  The grid never exceeds one CTA (pair) per SM (TPC).
@@ -725,13 +896,13 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, ns_tc_kernel_of<kShape>(), p);
+  e = cudaLaunchKernelEx(&cfg, kernel, p);
   if (e != cudaSuccess && kCluster) {
     // Cluster kernels may not take the cooperative attribute; the grid is sized to the
     // device's resident-cluster count, so on an otherwise idle GPU all pairs are resident.
     (void)cudaGetLastError();
     cfg.numAttrs = 0;
-    e = cudaLaunchKernelEx(&cfg, ns_tc_kernel_of<kShape>(), p);
+    e = cudaLaunchKernelEx(&cfg, kernel, p);
   }
   return e;
 }
@@ -739,11 +910,11 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
 }  // namespace
 
 cudaError_t prepare_ns_kernels(int* max_pairs, int* max_singles) {
-  const void* fns[3] = {(const void*)ns_tc_single_kernel, (const void*)ns_tc_pair_kernel,
-                        (const void*)ns_tc_mcast_kernel};
-  const int smems[3] = {Cfg<kShapeSingle>::SMEM_BYTES, Cfg<kShapePair>::SMEM_BYTES,
-                        Cfg<kShapeMcast>::SMEM_BYTES};
-  for (int k = 0; k < 3; ++k) {
+  const void* fns[4] = {(const void*)ns_tc_single_kernel, (const void*)ns_tc_pair_kernel,
+                        (const void*)ns_tc_mcast_kernel, (const void*)ns_tc_split_kernel};
+  const int smems[4] = {Cfg<kShapeSingle>::SMEM_BYTES, Cfg<kShapePair>::SMEM_BYTES,
+                        Cfg<kShapeMcast>::SMEM_BYTES, Cfg<kShapePair, true>::SMEM_BYTES};
+  for (int k = 0; k < 4; ++k) {
     const void* fn = fns[k];
     const int smem = smems[k];
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -759,16 +930,17 @@ cudaError_t prepare_ns_kernels(int* max_pairs, int* max_singles) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   *max_singles = per_sm * sms;
-  // Resident 2-CTA clusters: the smaller count of the two cluster kernels.
+  // Resident 2-CTA clusters: the smallest count of the cluster kernels.
   int n_min = 1 << 30;
-  for (int k = 1; k < 3; ++k) {
+  for (int k = 1; k < 4; ++k) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * 1024, 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smems[k];
     int n = 0;
-    e = k == 1 ? cudaOccupancyMaxActiveClusters(&n, ns_tc_pair_kernel, &cfg)
-               : cudaOccupancyMaxActiveClusters(&n, ns_tc_mcast_kernel, &cfg);
+    e = cudaOccupancyMaxActiveClusters(
+        &n, k == 1 ? ns_tc_pair_kernel : (k == 2 ? ns_tc_mcast_kernel : ns_tc_split_kernel),
+        &cfg);
     if (e != cudaSuccess) return e;
     n_min = n < n_min ? n : n_min;
   }
@@ -785,7 +957,9 @@ cudaError_t launch_ns_tc(const Plan& plan, const DevTables& dt, void* ws, int ns
   const int step = dt.tc_persistent ? nq : 1;
   for (int q0 = 0; q0 < nq; q0 += step) {
     const cudaError_t e =
-        dt.tc_shape == kShapePair
+        plan.ns_dtype == 2
+            ? launch_impl<kShapePair, true>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
+        : dt.tc_shape == kShapePair
             ? launch_impl<kShapePair>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
         : dt.tc_shape == kShapeMcast
             ? launch_impl<kShapeMcast>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
@@ -816,11 +990,13 @@ bool encode_tensor_maps(const Plan& plan, const void* ws, std::vector<CUtensorMa
   }
   maps->assign(plan.mats.size() * kMapsPerMat, CUtensorMap{});
   const uint8_t* base = static_cast<const uint8_t*>(ws);
+  const bool split = plan.ns_dtype == 2;  // three bf16 arrays per buffer, else one
+  const uint64_t esz = 2;
   auto make = [&](CUtensorMap* m, int64_t off, uint64_t inner, uint64_t outer, uint64_t pitch,
                   uint32_t box_inner, uint32_t box_outer,
                   CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) -> bool {
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {pitch * 2};
+    cuuint64_t strides[1] = {pitch * esz};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
@@ -841,6 +1017,27 @@ bool encode_tensor_maps(const Plan& plan, const void* ws, std::vector<CUtensorMa
     const MatDev& mt = plan.mats[i];
     CUtensorMap* m = maps->data() + i * kMapsPerMat;
     const int64_t xs[2] = {mt.x0, mt.x1};
+    if (split) {
+      // The same operand boxes as the bf16 path for each of the h, m and l arrays
+      // (slot + part * kMapPart); the epilogue writes with plain stores.
+      const int64_t xp = split_part_bytes((int64_t)mt.rows * mt.ldx * 2);
+      const int64_t ap = split_part_bytes((int64_t)mt.m * mt.lda * 2);
+      for (int part = 0; part < 3; ++part) {
+        CUtensorMap* mp = m + part * kMapPart;
+        for (int b = 0; b < 2; ++b) {
+          const int64_t o = xs[b] + part * xp;
+          if (!make(mp + 3 * b + 0, o, mt.cols, mt.rows, mt.ldx, 64, 128)) return false;
+          if (!make(mp + 3 * b + 1, o, mt.cols, mt.rows, mt.ldx, 64, 256)) return false;
+          if (!make(mp + 3 * b + 2, o, mt.cols, mt.rows, mt.ldx, 64, 64)) return false;
+        }
+        const int64_t ao = mt.a + part * ap, bo = mt.b + part * ap;
+        if (!make(mp + kMapAK128, ao, mt.m, mt.m, mt.lda, 64, 128)) return false;
+        if (!make(mp + kMapAK256, ao, mt.m, mt.m, mt.lda, 64, 256)) return false;
+        if (!make(mp + kMapBK128, bo, mt.m, mt.m, mt.lda, 64, 128)) return false;
+        if (!make(mp + kMapBK256, bo, mt.m, mt.m, mt.lda, 64, 256)) return false;
+      }
+      continue;
+    }
     for (int b = 0; b < 2; ++b) {
       if (!make(m + 3 * b + 0, xs[b], mt.cols, mt.rows, mt.ldx, 64, 128)) return false;
       if (!make(m + 3 * b + 1, xs[b], mt.cols, mt.rows, mt.ldx, 64, 256)) return false;

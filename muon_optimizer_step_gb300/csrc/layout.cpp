@@ -35,7 +35,8 @@ std::string build_plan(const int64_t* shapes, const uint8_t* is_matrix, int32_t 
   if (n_params < 0) return "n_params must be >= 0";
   if (n_params > 0 && shapes == nullptr) return "shapes is NULL";
   if (n_shards < 1 || n_shards > 128) return fmt("n_shards=%lld outside 1..128", n_shards);
-  if (ns_dtype != 0 && ns_dtype != 1) return fmt("ns_dtype=%lld is not 0 (bf16) or 1 (fp32)", ns_dtype);
+  if (ns_dtype < 0 || ns_dtype > 2)
+    return fmt("ns_dtype=%lld is not 0 (bf16), 1 (fp32) or 2 (split fp32)", ns_dtype);
   Plan p;
   p.n_params = n_params;
   p.n_shards = n_shards;
@@ -74,7 +75,8 @@ std::string build_plan(const int64_t* shapes, const uint8_t* is_matrix, int32_t 
   p.full_numel = full;
 
   // Matrices, their workspace buffers and chunk tables.
-  const int64_t esz = ns_dtype == 0 ? 2 : 4;
+  const int64_t esz = ns_dtype == 1 ? 4 : 2;
+  const int64_t parts = ns_dtype == 2 ? 3 : 1;  // split fp32: h, m and l bf16 arrays
   int64_t n_mats = 0;
   for (int32_t i = 0; i < n_params; ++i) n_mats += p.is_matrix[i];
   int64_t n_chunks = 0;
@@ -134,8 +136,8 @@ std::string build_plan(const int64_t* shapes, const uint8_t* is_matrix, int32_t 
   ws += (int64_t)p.mats.size() * 3 * 4;
   ws = round_up(ws, kWsAlign);
   for (MatDev& m : p.mats) {
-    const int64_t xb = round_up((int64_t)m.rows * m.ldx * esz, kWsAlign);
-    const int64_t ab = round_up((int64_t)m.m * m.lda * esz, kWsAlign);
+    const int64_t xb = round_up((int64_t)m.rows * m.ldx * esz, kWsAlign) * parts;
+    const int64_t ab = round_up((int64_t)m.m * m.lda * esz, kWsAlign) * parts;
     m.x0 = ws; ws += xb;
     m.x1 = ws; ws += xb;
     m.a = ws; ws += ab;

@@ -28,15 +28,17 @@ constexpr int kTcBK = 64;
 constexpr int kF32BM = 128;
 constexpr int kF32BN = 128;
 
-// Tensor maps per matrix on the bf16 path (index = mat * kMapsPerMat + slot).
+// Tensor maps per matrix on the tensor-core paths (index = mat * kMapsPerMat + slot).
 enum MapSlot {
   kMapX0K128 = 0, kMapX0K256 = 1, kMapX0MN = 2,
   kMapX1K128 = 3, kMapX1K256 = 4, kMapX1MN = 5,
   kMapAK128 = 6, kMapAK256 = 7,
   kMapBK128 = 8, kMapBK256 = 9,
-  // 32 x 32 boxes with 64-byte swizzle for the epilogue's TMA stores
+  // bf16: 32 x 32 boxes with 64-byte swizzle for the epilogue's TMA stores
   kMapX0St = 10, kMapX1St = 11, kMapASt = 12, kMapBSt = 13,
-  kMapsPerMat = 14
+  // split fp32: slots 0-9 map the h arrays, slot + kMapPart the m, + 2 kMapPart the l
+  kMapPart = 14,
+  kMapsPerMat = 42
 };
 
 enum Phase { kPhaseGram = 0, kPhasePoly = 1, kPhaseUpdate = 2 };
@@ -85,7 +87,7 @@ struct TileList {
 struct Plan {
   int32_t n_params = 0;
   int32_t n_shards = 1;
-  int32_t ns_dtype = 0;               // 0 bf16, 1 fp32
+  int32_t ns_dtype = 0;               // 0 bf16, 1 fp32, 2 split fp32 (bf16 x 3)
   int64_t N = 0;                      // flat elements
   int64_t L = 0;                      // shard length
   int64_t full_numel = 0;

@@ -45,6 +45,62 @@ __device__ __forceinline__ float4 load4(const float* p) {
 __device__ __forceinline__ float load1(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ float load1(const float* p) { return *p; }
 
+// An X buffer of split fp32 values: the h array and the distance (elements) from each
+// part's array to the next one's (h, m, l).
+struct SplitPtr {
+  __nv_bfloat16* h;
+  int64_t part;
+};
+__device__ __forceinline__ SplitPtr operator+(SplitPtr a, int64_t k) { return {a.h + k, a.part}; }
+__device__ __forceinline__ void store4(SplitPtr p, float a, float b, float c, float d) {
+  const float v[4] = {a, b, c, d};
+  __nv_bfloat16 q[3][4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) split_bf16x3(v[e], q[0][e], q[1][e], q[2][e]);
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    uint2 u;
+    u.x = (uint32_t)__bfloat16_as_ushort(q[k][0]) | ((uint32_t)__bfloat16_as_ushort(q[k][1]) << 16);
+    u.y = (uint32_t)__bfloat16_as_ushort(q[k][2]) | ((uint32_t)__bfloat16_as_ushort(q[k][3]) << 16);
+    *reinterpret_cast<uint2*>(p.h + k * p.part) = u;
+  }
+}
+__device__ __forceinline__ void store1(SplitPtr p, float a) {
+  __nv_bfloat16 h, m, l;
+  split_bf16x3(a, h, m, l);
+  p.h[0] = h;
+  p.h[p.part] = m;
+  p.h[2 * p.part] = l;
+}
+__device__ __forceinline__ float4 load4(SplitPtr p) {
+  const float4 h = load4(static_cast<const __nv_bfloat16*>(p.h));
+  const float4 m = load4(static_cast<const __nv_bfloat16*>(p.h + p.part));
+  const float4 l = load4(static_cast<const __nv_bfloat16*>(p.h + 2 * p.part));
+  return make_float4(h.x + (m.x + l.x), h.y + (m.y + l.y), h.z + (m.z + l.z),
+                     h.w + (m.w + l.w));
+}
+__device__ __forceinline__ float load1(SplitPtr p) {
+  return __bfloat162float(p.h[0]) +
+         (__bfloat162float(p.h[p.part]) + __bfloat162float(p.h[2 * p.part]));
+}
+
+// The X buffer at workspace byte offset `off` of matrix mt, as element type XT.
+template <typename XT>
+struct XBuf {
+  using ptr = XT*;
+  __device__ static ptr at(const uint8_t* ws, int64_t off, const MatDev&) {
+    return reinterpret_cast<XT*>(const_cast<uint8_t*>(ws) + off);
+  }
+};
+template <>
+struct XBuf<Bf16x3> {
+  using ptr = SplitPtr;
+  __device__ static ptr at(const uint8_t* ws, int64_t off, const MatDev& mt) {
+    return {reinterpret_cast<__nv_bfloat16*>(const_cast<uint8_t*>(ws) + off),
+            split_part_bytes((int64_t)mt.rows * mt.ldx * 2) / 2};
+  }
+};
+
 // Fixed-shape block sum (same order every run); the result is valid in thread 0.
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
@@ -102,13 +158,13 @@ momentum_input_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
     const MatDev& mt = mats[ch.mat];
     const float mu = gp.mu[mt.group];
     const int nesterov = gp.nesterov[mt.group];
-    XT* __restrict__ x = reinterpret_cast<XT*>(ws + mt.x0);
+    const typename XBuf<XT>::ptr x = XBuf<XT>::at(ws, mt.x0, mt);
     const int nv = ch.len >> 2;
     float ss = 0.f;
     if (ch.vec) {
       const float* g = G.p[ch.shard] + ch.shard_off;
       float* m = M.p[ch.shard] + ch.shard_off;
-      XT* xv = x + ch.local;
+      const typename XBuf<XT>::ptr xv = x + ch.local;
       const float4* g4 = reinterpret_cast<const float4*>(g);
       float4* m4 = reinterpret_cast<float4*>(m);
       int v = threadIdx.x;
@@ -208,7 +264,7 @@ full_input_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
     const ChunkDev ch = chunks[ci];
     const MatDev& mt = mats[ch.mat];
     const float* src = full + mt.full_off + ch.local;
-    XT* x = reinterpret_cast<XT*>(ws + mt.x0);
+    const typename XBuf<XT>::ptr x = XBuf<XT>::at(ws, mt.x0, mt);
     float ss = 0.f;
     for (int t = threadIdx.x; t < ch.len; t += kThreads) {
       const float v = src[t];
@@ -253,10 +309,10 @@ apply_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
     float lrs = gp.lr[mt.group] * mt.scale;
     const float decay = gp.decay[mt.group];
     if (pending_norm) lrs *= inv_norm[ch.mat];
-    const XT* __restrict__ o = reinterpret_cast<const XT*>(ws + (final_buf ? mt.x1 : mt.x0));
+    const typename XBuf<XT>::ptr o = XBuf<XT>::at(ws, final_buf ? mt.x1 : mt.x0, mt);
     if (ch.vec) {
       float* __restrict__ w = W.p[ch.shard] + ch.shard_off;
-      const XT* ov = o + ch.local;
+      const typename XBuf<XT>::ptr ov = o + ch.local;
       float4* w4 = reinterpret_cast<float4*>(w);
       const int nv = ch.len >> 2;
       int v = threadIdx.x;
@@ -344,7 +400,7 @@ export_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
     const ChunkDev ch = chunks[ci];
     const MatDev& mt = mats[ch.mat];
     const float s = pending_norm ? inv_norm[ch.mat] : 1.f;
-    const XT* x = reinterpret_cast<const XT*>(ws + (buf ? mt.x1 : mt.x0));
+    const typename XBuf<XT>::ptr x = XBuf<XT>::at(ws, buf ? mt.x1 : mt.x0, mt);
     float* dst = full + mt.full_off + ch.local;
     for (int t = threadIdx.x; t < ch.len; t += kThreads)
       dst[t] = load1(x + x_index(mt, ch.local + t)) * s;
@@ -369,8 +425,11 @@ cudaError_t launch_momentum_input(const Plan& plan, const DevTables& dt, const S
   if (plan.ns_dtype == 0)
     momentum_input_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
         dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, plan.L, w, partials, gp);
-  else
+  else if (plan.ns_dtype == 1)
     momentum_input_kernel<float><<<grid, kThreads, 0, st>>>(
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, plan.L, w, partials, gp);
+  else
+    momentum_input_kernel<Bf16x3><<<grid, kThreads, 0, st>>>(
         dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, plan.L, w, partials, gp);
   return cudaGetLastError();
 }
@@ -384,9 +443,12 @@ cudaError_t launch_full_input(const Plan& plan, const DevTables& dt, const float
   if (plan.ns_dtype == 0)
     full_input_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
         dt.chunks, (int64_t)plan.chunks.size(), dt.mats, full, w, partials);
-  else
+  else if (plan.ns_dtype == 1)
     full_input_kernel<float><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
                                                         dt.mats, full, w, partials);
+  else
+    full_input_kernel<Bf16x3><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
+                                                         dt.mats, full, w, partials);
   return cudaGetLastError();
 }
 
@@ -413,10 +475,14 @@ cudaError_t launch_apply(const Plan& plan, const DevTables& dt, const ShardPtrs&
     apply_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
         dt.chunks, (int64_t)plan.chunks.size(), dt.mats, wp, plan.L, w, final_buf, inv,
         pending_norm, gp);
-  else
+  else if (plan.ns_dtype == 1)
     apply_kernel<float><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
                                                    dt.mats, wp, plan.L, w, final_buf, inv,
                                                    pending_norm, gp);
+  else
+    apply_kernel<Bf16x3><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
+                                                    dt.mats, wp, plan.L, w, final_buf, inv,
+                                                    pending_norm, gp);
   return cudaGetLastError();
 }
 
@@ -447,9 +513,12 @@ cudaError_t launch_export(const Plan& plan, const DevTables& dt, const void* ws,
   if (plan.ns_dtype == 0)
     export_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
         dt.chunks, (int64_t)plan.chunks.size(), dt.mats, w, buf, inv, pending_norm, full);
-  else
+  else if (plan.ns_dtype == 1)
     export_kernel<float><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
                                                     dt.mats, w, buf, inv, pending_norm, full);
+  else
+    export_kernel<Bf16x3><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
+                                                     dt.mats, w, buf, inv, pending_norm, full);
   return cudaGetLastError();
 }
 

@@ -66,6 +66,10 @@ def test_workspace_bytes_cover_buffers():
     assert lay.workspace_bytes >= 2 * 256 * 128 * 2 + 2 * 128 * 128 * 2
     lay32 = capi.muon_layout_create([(256, 128)], 1, capi.MUON_NS_FP32)
     assert lay32.workspace_bytes >= 2 * 256 * 128 * 4 + 2 * 128 * 128 * 4
+    # split fp32: every buffer as three bf16 parts (h, m, l)
+    lay3 = capi.muon_layout_create([(256, 128)], 1, capi.MUON_NS_SPLIT_FP32)
+    assert lay3.workspace_bytes >= 3 * (2 * 256 * 128 * 2 + 2 * 128 * 128 * 2)
+    assert lay3.workspace_bytes - lay.workspace_bytes == 2 * (2 * 256 * 128 * 2 + 2 * 128 * 128 * 2)
 
 
 @pytest.mark.parametrize("shapes,n_shards,dtype,flags", [
@@ -73,7 +77,7 @@ def test_workspace_bytes_cover_buffers():
     ([(5, -1)], 1, 0, None),         # negative
     ([(4, 4)], 0, 0, None),          # no shards
     ([(4, 4)], 129, 0, None),        # too many shards
-    ([(4, 4)], 1, 2, None),          # unknown dtype
+    ([(4, 4)], 1, 3, None),          # unknown dtype
     ([(70000, 70000)], 1, 0, None),  # > 2^31 - 1 elements in one matrix
 ])
 def test_layout_rejects_bad_arguments(shapes, n_shards, dtype, flags):

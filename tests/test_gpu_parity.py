@@ -4,9 +4,11 @@ Tolerances (relative Frobenius error ||gpu - oracle|| / ||oracle||, per matrix):
   * gather / scatter, non-matrix bytes, shard padding: bit-exact;
   * momentum M and weights W: 1e-6 (fp32 arithmetic, one or two roundings per element);
   * stored orthogonalization input X: 2e-3 on the bf16 path (round-to-nearest bf16 has
-    relative error <= 2^-9 per element), 1e-6 on the fp32 path;
-  * Newton-Schulz output: 2e-2 on the bf16 path, 1e-4 on the fp32 path, both against the
-    oracle run on the GPU's own stored input and against the oracle's own input.
+    relative error <= 2^-9 per element), 1e-6 on the fp32 and split-fp32 paths (the latter
+    keeps h + m + l, within 2^-26 of each value);
+  * Newton-Schulz output: 2e-2 on the bf16 path, 1e-4 on the fp32 and split-fp32 paths, both
+    against the oracle run on the GPU's own stored input and against the oracle's own
+    input.
 W is compared as oracle_apply(W_before, O_gpu) against W_gpu, so the NS tolerance does not
 leak into the 1e-6 weight check.
 """
@@ -19,8 +21,8 @@ pytestmark = pytest.mark.gpu
 from oracle import muon_ref as ref  # noqa: E402
 from muon_optimizer_step_gb300 import inputs  # noqa: E402
 
-TOL_NS = {0: 2e-2, 1: 1e-4}
-TOL_X = {0: 2e-3, 1: 1e-6}
+TOL_NS = {0: 2e-2, 1: 1e-4, 2: 1e-4}
+TOL_X = {0: 2e-3, 1: 1e-6, 2: 1e-6}
 TOL_STATE = 1e-6
 
 
@@ -141,7 +143,8 @@ def recipe_inputs(wl, seed):
 # The 2e-2 bound of the bf16 path holds for gradient-like inputs; with singular values
 # spread over three decades, bf16 rounding of X, A and B alone (emulated on the CPU)
 # gives 4e-2 to 1e-1, so that family is checked on the fp32 path only.
-@pytest.mark.parametrize("ns_dtype,family", [(0, "recipe"), (1, "recipe"), (1, "spectrum")])
+@pytest.mark.parametrize("ns_dtype,family", [(0, "recipe"), (1, "recipe"), (1, "spectrum"),
+                                             (2, "recipe"), (2, "spectrum")])
 @pytest.mark.parametrize("ns_steps", [5, 1, 0])
 def test_orthogonalize_full_vs_oracle(capi, ns_dtype, family, ns_steps):
     wl = inputs.WORKLOADS["ragged_small"]
@@ -159,7 +162,7 @@ def test_orthogonalize_full_vs_oracle(capi, ns_dtype, family, ns_steps):
         assert e < TOL_NS[ns_dtype], (i, wl.shapes[i], e)
 
 
-@pytest.mark.parametrize("ns_dtype", [0, 1])
+@pytest.mark.parametrize("ns_dtype", [0, 1, 2])
 def test_orthogonalize_zero_matrix_gives_zero(capi, ns_dtype):
     shapes = [(130, 300), (5, 5)]
     lay = capi.muon_layout_create(shapes, 1, ns_dtype)
@@ -231,18 +234,18 @@ def run_steps(capi, wl, n_shards, ns_dtype, n_steps, check):
     return lay, W, M
 
 
-@pytest.mark.parametrize("ns_dtype", [0, 1])
+@pytest.mark.parametrize("ns_dtype", [0, 1, 2])
 def test_single_256x128_three_steps(capi, ns_dtype):
     run_steps(capi, inputs.WORKLOADS["single_256x128"], 1, ns_dtype, 3, None)
 
 
-@pytest.mark.parametrize("ns_dtype", [0, 1])
+@pytest.mark.parametrize("ns_dtype", [0, 1, 2])
 @pytest.mark.parametrize("n_shards", [1, 3])
 def test_ragged_two_steps(capi, ns_dtype, n_shards):
     run_steps(capi, inputs.WORKLOADS["ragged_small"], n_shards, ns_dtype, 2, None)
 
 
-@pytest.mark.parametrize("ns_dtype", [0, 1])
+@pytest.mark.parametrize("ns_dtype", [0, 1, 2])
 def test_step_equals_stages_and_sharding_is_exact(capi, ns_dtype):
     """muon_step = stage 1 + muon_orthogonalize_apply, bit for bit; 1 vs 5 shards bit for
     bit; and against the three separate stages: equal on the fp32 path, and on the bf16
@@ -285,10 +288,13 @@ def test_step_equals_stages_and_sharding_is_exact(capi, ns_dtype):
         return
     o = ref.flat_layout(wl.shapes, 1, wl.is_matrix)
     O = full_to_mats(O_last, capi.muon_layout_create(wl.shapes, 1, 0, wl.is_matrix), wl)
+    # per step, the staged apply reads O rounded to bf16 (2^-8 of each element) or, on
+    # the split-fp32 path, as h + m + l (2^-26)
+    factor = 2.0 ** -7 if ns_dtype == 0 else 2.0 ** -20
     for i, Oi in O.items():
         r, c = wl.shapes[i]
         sl = slice(o["offsets"][i], o["offsets"][i] + r * c)
-        bound = wl.lr * ref.update_scale(r, c) * 2.0 ** -7 * np.linalg.norm(Oi) \
+        bound = wl.lr * ref.update_scale(r, c) * factor * np.linalg.norm(Oi) \
             + 1e-6 * np.linalg.norm(W_st[sl].astype(np.float64))
         diff = np.linalg.norm(results[0][0][sl].astype(np.float64) - W_st[sl])
         assert diff <= bound, (i, diff, bound)
@@ -375,14 +381,15 @@ def test_each_tcgen05_variant_vs_oracle(capi, variant, persistent, monkeypatch):
 GROUP_HP = [(0.02, 0.01, 0.95, True), (0.05, 0.0, 0.9, False), (0.001, 0.1, 0.5, True)]
 
 
-def test_grouped_step_fp32_vs_oracle(capi):
-    """Per-group lr / wd / mu / Nesterov on the fp32 path, stage by stage against the
-    oracle's grouped step (momentum and weights 1e-6, update 1e-4)."""
+@pytest.mark.parametrize("ns_dtype", [1, 2])
+def test_grouped_step_fp32_vs_oracle(capi, ns_dtype):
+    """Per-group lr / wd / mu / Nesterov on the fp32 and split-fp32 paths, stage by stage
+    against the oracle's grouped step (momentum and weights 1e-6, update 1e-4)."""
     wl = inputs.WORKLOADS["ragged_small"]
     W0, Gs, M0 = inputs.host_inputs(wl)
     M0 = (np.random.default_rng(1).normal(0, 1e-3, M0.size)).astype(np.float32)
     group_of = [i % 3 for i in range(len(wl.shapes))]
-    lay = capi.muon_layout_create(wl.shapes, 3, 1, wl.is_matrix)
+    lay = capi.muon_layout_create(wl.shapes, 3, ns_dtype, wl.is_matrix)
     capi.muon_layout_set_groups(lay, group_of, 3)
     ws = capi.workspace_tensor(lay)
     W, M, G = split_shards(W0, 3), split_shards(M0, 3), split_shards(Gs[0], 3)
@@ -401,7 +408,7 @@ def test_grouped_step_fp32_vs_oracle(capi):
             continue
         lr, wd, mu, nest = GROUP_HP[group_of[i]]
         assert rel(Mg[sl], M_or[sl]) < TOL_STATE, i
-        assert rel(Og[i], upd[i]) < TOL_NS[1], i
+        assert rel(Og[i], upd[i]) < TOL_NS[ns_dtype], i
         want = ref.apply_update(ref.weight_decay(W0[sl], lr, wd), Og[i].reshape(-1), lr, r, c)
         assert rel(Wg[sl], want) < TOL_STATE, i
 
@@ -500,3 +507,27 @@ def test_fused_tail_each_variant(capi, variant, persistent, monkeypatch):
         assert diff <= bound, (variant, persistent, i, diff, bound)
     v = o["offsets"][1]
     assert np.array_equal(res["step"][0][v:v + 37], W0[v:v + 37])
+
+
+def test_split_fp32_matches_fp32_path_on_pair_tiles(capi):
+    """The split-fp32 tensor-core path against the fp32 CUDA-core path and the oracle on
+    shapes spanning several 256 x 256 pair tiles with ragged edges (tall, wide, square),
+    spread spectra: both within 1e-4 of the oracle, and of each other."""
+    shapes = [(600, 1100), (1100, 600), (520, 520), (257, 129), (7, 3), (64, 1000)]
+    wl = inputs.Workload("tf_mixed", tuple(shapes), (True,) * len(shapes), 1, seed=12, rank=4)
+    X = spectrum_inputs(wl, 21)
+    got = {}
+    for dt in (1, 2):
+        lay = capi.muon_layout_create(wl.shapes, 1, dt, wl.is_matrix)
+        if dt == 2:
+            k = capi.muon_layout_ns_kernel(lay)
+            assert k["tile_shape"] == 2 and not k["persistent"], k
+        ws = capi.workspace_tensor(lay)
+        out = torch.zeros(lay.full_numel, device="cuda")
+        capi.muon_orthogonalize_full(lay, ws, mats_to_full(X, lay), out, 5)
+        capi.muon_check()
+        got[dt] = full_to_mats(out, lay, wl)
+    for i, Xi in X.items():
+        want = ref.newton_schulz(Xi.astype(np.float32).astype(np.float64), 5)
+        assert rel(got[2][i], want) < TOL_NS[2], (wl.shapes[i], rel(got[2][i], want))
+        assert rel(got[2][i], got[1][i]) < TOL_NS[2], wl.shapes[i]
