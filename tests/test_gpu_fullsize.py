@@ -1,6 +1,6 @@
 """GPU parity at full size: the Llama-3-8B matrix set (224 matrices, 6.98e9 elements per
 fp32 buffer) in the launch configuration bench.py times, and its 8-shard variant with
-straddling parameters (bf16 and fp32 Newton-Schulz).
+straddling parameters (bf16, fp32 and split-fp32 Newton-Schulz).
 
 The oracle cannot run the whole step, so the checks are (a) bit-exact gather / scatter
 over every element, (b) momentum and weights on a seeded sample of a million flat
@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 from oracle import muon_ref as ref  # noqa: E402
 from muon_optimizer_step_gb300 import inputs  # noqa: E402
 
-TOL_NS = {0: 2e-2, 1: 1e-4}
+TOL_NS = {0: 2e-2, 1: 1e-4, 2: 1e-4}
 TOL_STATE = 1e-6
 LAYER = 7  # q, o, k, v, gate, up, down
 
@@ -136,3 +136,9 @@ def test_llama_8_shards_straddling_bf16(capi):
 
 def test_llama_8_shards_fp32_ns(capi):
     run_full(capi, "llama3_8b_8shards", 1, [1 + 0 * LAYER + 2, 1 + 9 * LAYER + 1])
+
+
+def test_llama_8_shards_split_fp32_ns(capi):
+    # layer 2's gate (tall: MN-major Gram operands), layer 3's down projection (wide,
+    # straddling shards 0 and 1: MN-major Update operand)
+    run_full(capi, "llama3_8b_8shards", 2, [1 + 2 * LAYER + 4, 1 + 3 * LAYER + 6])
