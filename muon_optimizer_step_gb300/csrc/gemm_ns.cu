@@ -50,10 +50,20 @@ constexpr int BN = 256;             // output tile columns
 constexpr int TMEM_COLS = 512;      // two 128 x 256 fp32 accumulators
 constexpr float kA = 3.4445f, kB = -4.7750f, kC = 2.0315f;
 
-// kSplit: the split-fp32 form (every fp32 operand kept as three bf16 parts h, m, l; six
-// kind::f16 MMAs per product: hh + hm + mh + hl + lh + mm); otherwise one bf16 operand.
-template <int kShape, bool kSplit = false>
+// Kernel variants of one tile shape:
+//   kVarTma:   bf16 operands; the epilogue stages 32 x 32 blocks in shared memory for TMA
+//              bulk stores;
+//   kVarSplit: the split-fp32 form: every fp32 operand kept as three bf16 parts h, m, l,
+//              six kind::f16 MMAs per product (hh + hm + mh + hl + lh + mm); plain-store
+//              epilogue.
+// (A bf16 pair variant that traded the staging buffers for a seventh operand stage and a
+// plain-store epilogue measured 3-20% slower than kVarTma: the stores cost more than the
+// deeper pipeline saves.)
+constexpr int kVarTma = 0, kVarSplit = 1;
+
+template <int kShape, int kVar = kVarTma>
 struct Cfg {
+  static constexpr bool kSplit = kVar == kVarSplit;
   static constexpr bool kCluster = kShape != kShapeSingle;  // a 2-CTA cluster per tile
   static constexpr bool kTwoSm = kShape == kShapePair;      // tcgen05 cta_group::2
   static constexpr int BK = 64;                       // k-block: one 128-byte row of bf16
@@ -70,10 +80,12 @@ struct Cfg {
   static constexpr int A_BYTES = A_PART * PARTS;
   static constexpr int B_BYTES = B_PART * PARTS;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGING = kVar == kVarTma ? EPI_WARPS * 4096 : 0;  // 4 KB per warp
   static constexpr int STAGES = kTwoSm ? (kSplit ? 2 : 6) : 4;
-  static_assert(!kSplit || kTwoSm, "the split-fp32 form runs on CTA pairs only");
-  // operand stages, 4 KB of epilogue staging per epilogue warp, alignment, barriers
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * 4096 + 1024 + 256;
+  static_assert(kVar == kVarTma || kTwoSm, "the plain-store variants run on CTA pairs only");
+  // operand stages, epilogue staging, alignment, barriers
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING + 1024 + 256;
+  static_assert(SMEM_BYTES <= 232448, "more than the 227 KB of shared memory a CTA can have");
 };
 
 struct NsParams {
@@ -307,73 +319,87 @@ __device__ __forceinline__ void epilogue_block(const NsParams& p, const MatDev& 
   st.pending = true;
 }
 
-// ---------------------------------------------------------------- split-fp32 epilogue
-// Row run of 32 split values at element index e of a buffer whose m and l arrays are
-// `part` elements after its h array: loads h + (m + l), or stores the split of f.
-// n < 32 takes the first n only.
+// ---------------------------------------------------------------- plain-store epilogue
+// Values kept as P bf16 parts in P equal arrays, `part` elements apart: P = 1 is plain
+// bf16, P = 3 the split-fp32 form (h, m, l).
+template <int P>
+__device__ __forceinline__ void split_parts(float x, __nv_bfloat16 (&q)[P]) {
+  if constexpr (P == 1) q[0] = __float2bfloat16_rn(x);
+  else split_bf16x3(x, q[0], q[1], q[2]);
+}
+
+// Row run of 32 values at element index e: loads the sum of the parts, or stores the
+// parts of f.  n < 32 takes the first n only.
+template <int P>
 __device__ __forceinline__ void load_split_run(const __nv_bfloat16* h, int64_t part, int64_t e,
                                                int n, float (&x)[32]) {
   if (n == 32) {
-    uint4 u[3][4];
 #pragma unroll
-    for (int k = 0; k < 3; ++k)
+    for (int t = 0; t < 32; ++t) x[t] = 0.f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) u[k][q] = *reinterpret_cast<const uint4*>(h + k * part + e + 8 * q);
-    float hf[32], mf[32], lf[32];
-    unpack_bf16x32(u[0], hf);
-    unpack_bf16x32(u[1], mf);
-    unpack_bf16x32(u[2], lf);
+    for (int k = P - 1; k >= 0; --k) {  // smallest part first
+      uint4 u[4];
 #pragma unroll
-    for (int t = 0; t < 32; ++t) x[t] = hf[t] + (mf[t] + lf[t]);
+      for (int q = 0; q < 4; ++q) u[q] = *reinterpret_cast<const uint4*>(h + k * part + e + 8 * q);
+      float v[32];
+      unpack_bf16x32(u, v);
+#pragma unroll
+      for (int t = 0; t < 32; ++t) x[t] = v[t] + x[t];
+    }
   } else {
 #pragma unroll
-    for (int t = 0; t < 32; ++t)
-      x[t] = t < n ? __bfloat162float(h[e + t]) + (__bfloat162float(h[part + e + t]) +
-                                                   __bfloat162float(h[2 * part + e + t]))
-                   : 0.f;
+    for (int t = 0; t < 32; ++t) {
+      float v = 0.f;
+#pragma unroll
+      for (int k = P - 1; k >= 0; --k) v = (t < n ? __bfloat162float(h[k * part + e + t]) : 0.f) + v;
+      x[t] = v;
+    }
   }
 }
 
+template <int P>
 __device__ __forceinline__ void store_split1(__nv_bfloat16* h, int64_t part, int64_t e, float f) {
-  __nv_bfloat16 hb, mb, lb;
-  split_bf16x3(f, hb, mb, lb);
-  h[e] = hb;
-  h[part + e] = mb;
-  h[2 * part + e] = lb;
+  __nv_bfloat16 q[P];
+  split_parts<P>(f, q);
+#pragma unroll
+  for (int k = 0; k < P; ++k) h[k * part + e] = q[k];
 }
 
+template <int P>
 __device__ __forceinline__ void store_split_run(__nv_bfloat16* h, int64_t part, int64_t e, int n,
                                                 const float (&f)[32]) {
   if (n == 32) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      uint32_t w[3][4];
+      uint32_t w[P][4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        __nv_bfloat16 h0, m0, l0, h1, m1, l1;
-        split_bf16x3(f[8 * q + 2 * k], h0, m0, l0);
-        split_bf16x3(f[8 * q + 2 * k + 1], h1, m1, l1);
-        w[0][k] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-        w[1][k] = (uint32_t)__bfloat16_as_ushort(m0) | ((uint32_t)__bfloat16_as_ushort(m1) << 16);
-        w[2][k] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+        __nv_bfloat16 a[P], b[P];
+        split_parts<P>(f[8 * q + 2 * k], a);
+        split_parts<P>(f[8 * q + 2 * k + 1], b);
+#pragma unroll
+        for (int c = 0; c < P; ++c)
+          w[c][k] = (uint32_t)__bfloat16_as_ushort(a[c]) | ((uint32_t)__bfloat16_as_ushort(b[c]) << 16);
       }
 #pragma unroll
-      for (int k = 0; k < 3; ++k)
-        *reinterpret_cast<uint4*>(h + k * part + e + 8 * q) = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
+      for (int c = 0; c < P; ++c)
+        *reinterpret_cast<uint4*>(h + c * part + e + 8 * q) = make_uint4(w[c][0], w[c][1], w[c][2], w[c][3]);
     }
   } else {
 #pragma unroll
     for (int t = 0; t < 32; ++t)
-      if (t < n) store_split1(h, part, e + t, f[t]);
+      if (t < n) store_split1<P>(h, part, e + t, f[t]);
   }
 }
 
-// Epilogue of a 32 x 32 block on the split-fp32 path: the same arithmetic as
-// epilogue_block on fp32 values (inputs h + m + l), written back as three bf16 parts with
-// plain stores: the row run of each lane, and for symmetric outputs the transposed block,
-// whose stores are coalesced across the warp (lane = column of the mirror row).  Diagonal
-// blocks keep the element rule (j >= i written, j > i mirrored).
-__device__ __forceinline__ void epilogue_block_split(const NsParams& p, const MatDev& mt,
+// Epilogue of a 32 x 32 block with plain stores: the same arithmetic as epilogue_block
+// on fp32 values (inputs: the sum of the P parts), written back as P bf16 parts: the row
+// run of each lane, and for symmetric outputs the transposed block, whose stores are
+// coalesced across the warp (lane = column of the mirror row).  Diagonal blocks keep the
+// element rule (j >= i written, j > i mirrored).  It needs no shared memory, which leaves
+// room for the split form's wider stages.
+template <int P>
+__device__ __forceinline__ void epilogue_block_plain(const NsParams& p, const MatDev& mt,
                                                      int phase, int x_in, bool apply, int r0,
                                                      int jb, int lane, const uint32_t (&acc)[32],
                                                      float s) {
@@ -387,11 +413,11 @@ __device__ __forceinline__ void epilogue_block_split(const NsParams& p, const Ma
     const int n = i < mt.rows ? min(32, mt.cols - jb) : 0;
     const int64_t e = (int64_t)i * mt.ldx + jb;
     float x[32];
-    load_split_run(xin, part, e, n, x);
+    load_split_run<P>(xin, part, e, n, x);
 #pragma unroll
     for (int t = 0; t < 32; ++t) f[t] = s * fmaf(kA, x[t], __uint_as_float(acc[t]));
     if (apply && n > 0) apply_row_run(p.ap, mt, i, jb, n, f);
-    if (n > 0) store_split_run(xout, part, e, n, f);
+    if (n > 0) store_split_run<P>(xout, part, e, n, f);
     return;
   }
   if (r0 >= mt.m || jb >= mt.m || jb < r0) return;  // outside, or below the diagonal
@@ -404,7 +430,7 @@ __device__ __forceinline__ void epilogue_block_split(const NsParams& p, const Ma
     for (int t = 0; t < 32; ++t) f[t] = __uint_as_float(acc[t]) * s;
   } else {
     float a[32];
-    load_split_run(am, part, e, n, a);
+    load_split_run<P>(am, part, e, n, a);
 #pragma unroll
     for (int t = 0; t < 32; ++t) f[t] = fmaf(kB, a[t], kC * __uint_as_float(acc[t]));
   }
@@ -414,17 +440,17 @@ __device__ __forceinline__ void epilogue_block_split(const NsParams& p, const Ma
 #pragma unroll
       for (int t = 0; t < 32; ++t) {
         const int j = jb + t;
-        if (j >= i && j < mt.m) store_split1(out, part, (int64_t)i * mt.lda + j, f[t]);
-        if (j > i && j < mt.m) store_split1(out, part, (int64_t)j * mt.lda + i, f[t]);
+        if (j >= i && j < mt.m) store_split1<P>(out, part, (int64_t)i * mt.lda + j, f[t]);
+        if (j > i && j < mt.m) store_split1<P>(out, part, (int64_t)j * mt.lda + i, f[t]);
       }
     }
     return;
   }
-  if (n > 0) store_split_run(out, part, e, n, f);
+  if (n > 0) store_split_run<P>(out, part, e, n, f);
   if (i < mt.m) {
 #pragma unroll
     for (int t = 0; t < 32; ++t)
-      if (jb + t < mt.m) store_split1(out, part, (int64_t)(jb + t) * mt.lda + i, f[t]);
+      if (jb + t < mt.m) store_split1<P>(out, part, (int64_t)(jb + t) * mt.lda + i, f[t]);
   }
 }
 
@@ -464,9 +490,10 @@ __device__ __forceinline__ bool epi_any(bool v) {
   return r != 0;
 }
 
-template <int kShape, bool kSplit = false>
+template <int kShape, int kVar = kVarTma>
 __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
-  using C = Cfg<kShape, kSplit>;
+  using C = Cfg<kShape, kVar>;
+  constexpr bool kSplit = C::kSplit;
   constexpr bool kCluster = C::kCluster;
   constexpr bool kTwoSm = C::kTwoSm;
   extern __shared__ uint8_t smem_raw[];
@@ -474,7 +501,7 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* tiles_smem = smem_raw + pad;
   uint64_t* bars = reinterpret_cast<uint64_t*>(tiles_smem + C::STAGES * C::STAGE_BYTES +
-                                               EPI_WARPS * 4096);
+                                               C::STAGING);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
   uint64_t* acc_full = bars + 2 * C::STAGES;
@@ -752,11 +779,12 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
 #pragma unroll 1
             for (int c = c_first; c < c_last; ++c) {
               uint32_t v[32];
-              if constexpr (kSplit) {
+              if constexpr (kVar != kVarTma) {
                 tmem_ld_32x32b_x32(
                     tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * BN + 32 * c), v);
                 tmem_ld_wait();
-                epilogue_block_split(p, mt, phase, x_in, apply, r0, tile.j0 + 32 * c, lane, v, s);
+                epilogue_block_plain<C::PARTS>(p, mt, phase, x_in, apply, r0, tile.j0 + 32 * c,
+                                               lane, v, s);
               } else {
                 uint4 in_cur[4];
                 const bool have_cur = epilogue_prefetch(p, mt, phase, x_in, i, tile.j0 + 32 * c,
@@ -831,7 +859,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 // The split-fp32 form, on CTA pairs.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     ns_tc_split_kernel(const __grid_constant__ NsParams p) {
-  ns_tc_body<kShapePair, true>(p);
+  ns_tc_body<kShapePair, kVarSplit>(p);
 }
 
 using NsKernel = void (*)(NsParams);
@@ -855,7 +883,7 @@ __global__ void selftest_timeout_kernel(int* err, long long budget) {
   if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, budget, err, &abort_flag);
 }
 
-template <int kShape, bool kSplit = false>
+template <int kShape, int kVar = kVarTma>
 cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_steps,
                         int q_begin, int q_end, long long budget, const ApplyArgs* ap,
                         cudaStream_t st) {
@@ -883,11 +911,11 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  constexpr bool kCluster = Cfg<kShape, kSplit>::kCluster;
-  const NsKernel kernel = kSplit ? ns_tc_split_kernel : ns_tc_kernel_of<kShape>();
+  constexpr bool kCluster = Cfg<kShape, kVar>::kCluster;
+  const NsKernel kernel = kVar == kVarSplit ? ns_tc_split_kernel : ns_tc_kernel_of<kShape>();
   cfg.gridDim = dim3((unsigned)((kCluster ? 2 : 1) * dt.tc_units), 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<kShape, kSplit>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = Cfg<kShape, kVar>::SMEM_BYTES;
   cfg.stream = st;
   // Cooperative: every CTA must be resident at once, because tiles wait on tiles of
   // other CTAs.  The grid never exceeds one CTA (pair) per SM (TPC).
@@ -913,7 +941,7 @@ cudaError_t prepare_ns_kernels(int* max_pairs, int* max_singles) {
   const void* fns[4] = {(const void*)ns_tc_single_kernel, (const void*)ns_tc_pair_kernel,
                         (const void*)ns_tc_mcast_kernel, (const void*)ns_tc_split_kernel};
   const int smems[4] = {Cfg<kShapeSingle>::SMEM_BYTES, Cfg<kShapePair>::SMEM_BYTES,
-                        Cfg<kShapeMcast>::SMEM_BYTES, Cfg<kShapePair, true>::SMEM_BYTES};
+                        Cfg<kShapeMcast>::SMEM_BYTES, Cfg<kShapePair, kVarSplit>::SMEM_BYTES};
   for (int k = 0; k < 4; ++k) {
     const void* fn = fns[k];
     const int smem = smems[k];
@@ -938,9 +966,10 @@ cudaError_t prepare_ns_kernels(int* max_pairs, int* max_singles) {
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smems[k];
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(
-        &n, k == 1 ? ns_tc_pair_kernel : (k == 2 ? ns_tc_mcast_kernel : ns_tc_split_kernel),
-        &cfg);
+    const NsKernel kern = k == 1 ? ns_tc_pair_kernel
+                          : k == 2 ? ns_tc_mcast_kernel
+                                   : ns_tc_split_kernel;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
     if (e != cudaSuccess) return e;
     n_min = n < n_min ? n : n_min;
   }
@@ -958,7 +987,7 @@ cudaError_t launch_ns_tc(const Plan& plan, const DevTables& dt, void* ws, int ns
   for (int q0 = 0; q0 < nq; q0 += step) {
     const cudaError_t e =
         plan.ns_dtype == 2
-            ? launch_impl<kShapePair, true>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
+            ? launch_impl<kShapePair, kVarSplit>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
         : dt.tc_shape == kShapePair
             ? launch_impl<kShapePair>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
         : dt.tc_shape == kShapeMcast
