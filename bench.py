@@ -15,6 +15,7 @@ Under torchrun (N > 1) every rank runs its own replica of the workload on its ow
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import math
 import os
@@ -114,6 +115,10 @@ def ns_kernel_label(kernel, ns_steps, ns_dtype="bf16"):
         "256x256 tiles)"
     return "%s, %d units, %d launch(es) per step; the last Update also applies W" % (
         name, kernel["units"], launches)
+
+
+# Process-group timeout of the multi-rank bench: far above any step, far below forever.
+PG_TIMEOUT_S = 600
 
 
 def load_peaks():
@@ -322,7 +327,10 @@ def run_ours(args):
     dist = None
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        # A rank that dies must not hold the others forever: their next collective
+        # fails after this timeout (tested on gloo ranks in tests/test_owners_and_ranks.py).
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local),
+                                timeout=datetime.timedelta(seconds=PG_TIMEOUT_S))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 

@@ -106,3 +106,46 @@ def test_two_gloo_ranks_agree_on_owner_plan_and_max_timing(tmp_path):
         agree, a, b = open(tmp_path / f"rank{r}.txt").read().split()
         assert agree == "1"
         assert float(a) == 2.0 and float(b) == 10.0
+
+
+def _rank_dies_main(rank, world, port, out_dir, timeout_s):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import datetime
+    import time
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=timeout_s))
+    import bench
+    if rank == 1:
+        # Leaves between steps: never joins the timing reduction.
+        os._exit(0)
+    t0 = time.monotonic()
+    try:
+        bench.reduce_max_over_ranks([1.0], dist, "cpu")
+        outcome = "returned"
+    except Exception as e:  # the surviving rank must get an error, not hang
+        outcome = "error:" + type(e).__name__
+    with open(os.path.join(out_dir, "rank0.txt"), "w") as f:
+        f.write(f"{outcome} {time.monotonic() - t0:.3f}\n")
+    os._exit(0)
+
+
+def test_surviving_rank_gets_an_error_when_a_rank_dies(tmp_path):
+    """Failure detection on the host: one of two gloo ranks exits instead of joining the
+    step-time reduction; the other's collective fails within the process-group timeout
+    instead of waiting forever (bench.py sets such a timeout on its NCCL group)."""
+    import torch.multiprocessing as mp
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    timeout_s = 10
+    mp.start_processes(_rank_dies_main, args=(2, port, str(tmp_path), timeout_s), nprocs=2,
+                       start_method="spawn")
+    outcome, elapsed = open(tmp_path / "rank0.txt").read().split()
+    assert outcome.startswith("error:"), outcome
+    assert float(elapsed) < 3 * timeout_s
+    import bench
+    assert 60 <= bench.PG_TIMEOUT_S <= 3600
