@@ -218,7 +218,7 @@ muon_status muon_export_update(const muon_layout* layout, const void* workspace,
  * that cannot afford the synchronisation cudaMalloc / cudaFree may imply, a plugin inside
  * a process where only the host application allocates device memory.
  *   layout    a layout created with ns_dtype = MUON_NS_FP32 (the fp32 CUDA-core path);
- *             bf16 layouts return MUON_ERR_UNSUPPORTED.
+ *             the tensor-core layouts (bf16, split fp32) return MUON_ERR_UNSUPPORTED.
  *   full_in   device, fp32 full layout (muon_full_offsets), 16-byte aligned: the inputs.
  *   full_out  device, same layout, 16-byte aligned: receives the orthogonalized updates.
  * Everything else (the layout's device tables and the workspace) lives in one file-scope
