@@ -672,7 +672,14 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
             const TileDev tile = p.tiles[phase][ti];
             const MatDev& mt = p.mats[tile.mat];
             const TileOps ops = tile_ops<kCluster>(mt, phase, it & 1);
-            const uint32_t idesc = idesc_bf16(C::MMA_M, BN, ops.a_mn, ops.b_mn);
+            // Symmetric phases: a CTA whose rows all lie at or below the tile's second
+            // column half (single CTAs with i0 = j0 + 128; the odd CTA of a multicast
+            // cluster on a diagonal tile) would compute its first 128 columns only for the
+            // epilogue to discard them: it runs N = 128 MMAs on the second half of B into
+            // the accumulator's second half instead.
+            const bool half_n = !kTwoSm && phase != kPhaseUpdate &&
+                                tile.j0 + 128 <= tile.i0 + (kCluster ? 128 * (int)rank : 0);
+            const uint32_t idesc = idesc_bf16(C::MMA_M, half_n ? BN / 2 : BN, ops.a_mn, ops.b_mn);
             const int ab = lt & 1;
             if (!wait_role<kCluster>(&acc_empty[ab], (uint32_t)(((lt >> 1) & 1) ^ 1), p, abort,
                                   peer_abort)) {
@@ -680,7 +687,7 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
               break;
             }
             tc_fence_after();
-            const uint32_t d = tmem_base + (uint32_t)(ab * BN);
+            const uint32_t d = tmem_base + (uint32_t)(ab * BN) + (half_n ? (uint32_t)(BN / 2) : 0u);
             for (int kb = 0; kb < tile.kblocks && ok; ++kb) {
               if (!wait_role<kCluster>(&full[stage], ph, p, abort, peer_abort)) {
                 ok = false;
@@ -688,7 +695,8 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
               }
               tc_fence_after();
               const uint32_t sa = sbase + stage * C::STAGE_BYTES;
-              const uint32_t sb = sa + C::A_BYTES;
+              // (the second half of B: rows 128-255 K-major, or MN-major boxes 2 and 3)
+              const uint32_t sb = sa + C::A_BYTES + (half_n ? (uint32_t)(C::B_PART / 2) : 0u);
               // One MMA reads 32 bytes of every operand row: +32 B along a K-major row, or
               // UMMA_K rows of 128 B of an MN-major box.
               constexpr uint32_t kMnStep = C::UMMA_K * 128;
