@@ -29,7 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-METRIC = "Muon step time (ms) and Newton-Schulz TFLOP/s + % bf16 peak at 1 GB300"
+METRIC = "Muon step time (ms) and Newton\u2013Schulz TFLOP/s + % bf16 peak at 1 GB300"
 DEFAULT_WORKLOAD = "llama3_8b_x32"
 
 
