@@ -925,21 +925,17 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = Cfg<kShape, kVar>::SMEM_BYTES;
   cfg.stream = st;
-  // Cooperative: every CTA must be resident at once, because tiles wait on tiles of
-  // other CTAs.  The grid never exceeds one CTA (pair) per SM (TPC).
+  // A persistent launch (several phases) needs every CTA resident at once, because tiles
+  // wait on tiles of other CTAs.  Single CTAs ask for a cooperative launch.  Cluster
+  // kernels are launched without that attribute, with a grid sized to the device's
+  // resident-cluster count (occupancy query), so that no launch can fail and be retried
+  // (which would also break stream capture).  One phase per launch needs neither.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = (q_end - q_begin > 1 && !kCluster) ? 1 : 0;
   e = cudaLaunchKernelEx(&cfg, kernel, p);
-  if (e != cudaSuccess && kCluster) {
-    // Cluster kernels may not take the cooperative attribute; the grid is sized to the
-    // device's resident-cluster count, so on an otherwise idle GPU all pairs are resident.
-    (void)cudaGetLastError();
-    cfg.numAttrs = 0;
-    e = cudaLaunchKernelEx(&cfg, kernel, p);
-  }
   return e;
 }
 

@@ -531,3 +531,42 @@ def test_split_fp32_matches_fp32_path_on_pair_tiles(capi):
         want = ref.newton_schulz(Xi.astype(np.float32).astype(np.float64), 5)
         assert rel(got[2][i], want) < TOL_NS[2], (wl.shapes[i], rel(got[2][i], want))
         assert rel(got[2][i], got[1][i]) < TOL_NS[2], wl.shapes[i]
+
+
+@pytest.mark.parametrize("ns_dtype,variant,persistent", [(0, None, None), (0, "2", "1"),
+                                                         (0, "1", "1"), (2, None, None)])
+def test_step_replays_from_a_cuda_graph(capi, ns_dtype, variant, persistent, monkeypatch):
+    """muon_step captured once in a CUDA graph (after a first eager call has prepared the
+    layout's tables and tensor maps) and replayed for two more steps gives the same bits
+    as three eager steps: per-phase launches, persistent launches of CTA pairs and of
+    single CTAs, and the split-fp32 path."""
+    if variant is not None:
+        monkeypatch.setenv("MUON_TC_KERNEL", variant)
+        monkeypatch.setenv("MUON_NS_PERSISTENT", persistent)
+    wl = inputs.WORKLOADS["ragged_small"]
+    W0, Gs, M0 = inputs.host_inputs(wl)
+    outs = []
+    for mode in ("eager", "graph"):
+        lay = capi.muon_layout_create(wl.shapes, 3, ns_dtype, wl.is_matrix)
+        ws = capi.workspace_tensor(lay)
+        W, M = split_shards(W0, 3), split_shards(M0, 3)
+        G = split_shards(Gs[0], 3)
+        capi.muon_step(W, G, M, lay, ws, wl.lr, wl.wd, wl.mu, True, 5)
+        capi.muon_check()
+        if mode == "eager":
+            for _ in range(2):
+                capi.muon_step(W, G, M, lay, ws, wl.lr, wl.wd, wl.mu, True, 5)
+        else:
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g):
+                    capi.muon_step(W, G, M, lay, ws, wl.lr, wl.wd, wl.mu, True, 5)
+            torch.cuda.current_stream().wait_stream(side)
+            for _ in range(2):
+                g.replay()
+        capi.muon_check()
+        outs.append((join_shards(W, lay.numel), join_shards(M, lay.numel)))
+    assert np.array_equal(outs[0][0], outs[1][0])
+    assert np.array_equal(outs[0][1], outs[1][1])
