@@ -672,13 +672,24 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
             const TileDev tile = p.tiles[phase][ti];
             const MatDev& mt = p.mats[tile.mat];
             const TileOps ops = tile_ops<kCluster>(mt, phase, it & 1);
-            // Symmetric phases: a CTA whose rows all lie at or below the tile's second
-            // column half (single CTAs with i0 = j0 + 128; the odd CTA of a multicast
-            // cluster on a diagonal tile) would compute its first 128 columns only for the
-            // epilogue to discard them: it runs N = 128 MMAs on the second half of B into
-            // the accumulator's second half instead.
-            const bool half_n = !kTwoSm && phase != kPhaseUpdate &&
-                                tile.j0 + 128 <= tile.i0 + (kCluster ? 128 * (int)rank : 0);
+            // Columns the epilogue would discard are not computed (CTAs that issue their
+            // own MMAs, i.e. all but CTA pairs):
+            //  - symmetric phases: a CTA whose rows all lie at or below the tile's second
+            //    column half (single CTAs with i0 = j0 + 128; the odd CTA of a multicast
+            //    cluster on a diagonal tile) skips the first half;
+            //  - a tile whose second column half lies outside the matrix skips that half;
+            //  - a CTA whose rows all lie outside the matrix (the odd CTA of a multicast
+            //    cluster on a ragged last row band) issues no MMAs, only the commits that
+            //    hand its stages back.
+            // A half is done as N = 128 MMAs on that half of B, into that half of the
+            // accumulator.
+            const int row0 = tile.i0 + (kCluster ? 128 * (int)rank : 0);
+            const int n_out = phase == kPhaseUpdate ? mt.cols : mt.m;
+            const int m_out = phase == kPhaseUpdate ? mt.rows : mt.m;
+            const bool skip_first = !kTwoSm && phase != kPhaseUpdate && tile.j0 + 128 <= row0;
+            const bool skip_second = !kTwoSm && tile.j0 + 128 >= n_out;
+            const bool idle = !kTwoSm && (row0 >= m_out || (skip_first && skip_second));
+            const bool half_n = !idle && (skip_first || skip_second);
             const uint32_t idesc = idesc_bf16(C::MMA_M, half_n ? BN / 2 : BN, ops.a_mn, ops.b_mn);
             const int ab = lt & 1;
             if (!wait_role<kCluster>(&acc_empty[ab], (uint32_t)(((lt >> 1) & 1) ^ 1), p, abort,
@@ -687,7 +698,7 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
               break;
             }
             tc_fence_after();
-            const uint32_t d = tmem_base + (uint32_t)(ab * BN) + (half_n ? (uint32_t)(BN / 2) : 0u);
+            const uint32_t d = tmem_base + (uint32_t)(ab * BN) + (skip_first ? (uint32_t)(BN / 2) : 0u);
             for (int kb = 0; kb < tile.kblocks && ok; ++kb) {
               if (!wait_role<kCluster>(&full[stage], ph, p, abort, peer_abort)) {
                 ok = false;
@@ -696,12 +707,13 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
               tc_fence_after();
               const uint32_t sa = sbase + stage * C::STAGE_BYTES;
               // (the second half of B: rows 128-255 K-major, or MN-major boxes 2 and 3)
-              const uint32_t sb = sa + C::A_BYTES + (half_n ? (uint32_t)(C::B_PART / 2) : 0u);
+              const uint32_t sb = sa + C::A_BYTES + (skip_first ? (uint32_t)(C::B_PART / 2) : 0u);
               // One MMA reads 32 bytes of every operand row: +32 B along a K-major row, or
               // UMMA_K rows of 128 B of an MN-major box.
               constexpr uint32_t kMnStep = C::UMMA_K * 128;
 #pragma unroll
               for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
+                if (idle) break;
                 const uint32_t koff_a = ops.a_mn ? kk * kMnStep : kk * 32;
                 const uint32_t koff_b = ops.b_mn ? kk * kMnStep : kk * 32;
                 const uint32_t lbo_a = ops.a_mn ? C::MN_BOX : 16;
