@@ -570,3 +570,64 @@ def test_step_replays_from_a_cuda_graph(capi, ns_dtype, variant, persistent, mon
         outs.append((join_shards(W, lay.numel), join_shards(M, lay.numel)))
     assert np.array_equal(outs[0][0], outs[1][0])
     assert np.array_equal(outs[0][1], outs[1][1])
+
+
+GUARD = 1 << 16
+
+
+def guarded_workspace(lay, fill):
+    """A workspace with GUARD bytes of `fill` on both sides, the workspace itself filled
+    with `fill` too (1024-byte aligned)."""
+    raw = torch.full((lay.workspace_bytes + 2 * GUARD + 1024,), fill, dtype=torch.uint8,
+                     device="cuda")
+    off = GUARD + (-(raw.data_ptr() + GUARD)) % 1024
+    ws = raw[off: off + lay.workspace_bytes]
+    return raw, off, ws
+
+
+@pytest.mark.parametrize("ns_dtype", [0, 1, 2])
+def test_workspace_guards_and_poisoned_workspace(capi, ns_dtype):
+    """No kernel writes outside the workspace or reads workspace bytes it has not written:
+    with the workspace and guard bands filled with 0xFF (NaN as fp32 and bf16), two steps
+    give the same bits as with a zeroed workspace, and the guard bands stay 0xFF."""
+    wl = inputs.WORKLOADS["ragged_small"]
+    W0, Gs, M0 = inputs.host_inputs(wl)
+    outs = []
+    for fill in (0, 0xFF):
+        lay = capi.muon_layout_create(wl.shapes, 3, ns_dtype, wl.is_matrix)
+        raw, off, ws = guarded_workspace(lay, fill)
+        W, M = split_shards(W0, 3), split_shards(M0, 3)
+        for t in range(2):
+            capi.muon_step(W, split_shards(Gs[t], 3), M, lay, ws, wl.lr, wl.wd, wl.mu, True, 5)
+        capi.muon_check()
+        if fill == 0xFF:
+            r = raw.cpu().numpy()
+            assert np.all(r[:off] == 0xFF)
+            assert np.all(r[off + lay.workspace_bytes:] == 0xFF)
+        outs.append((join_shards(W, lay.numel), join_shards(M, lay.numel)))
+    assert np.array_equal(outs[0][0], outs[1][0])
+    assert np.array_equal(outs[0][1], outs[1][1])
+
+
+@pytest.mark.parametrize("ns_dtype", [0, 2])
+def test_checkpoint_resume_is_bit_exact(capi, ns_dtype):
+    """Momentum is caller state: saving W and M after step 1 to the host and resuming in
+    fresh buffers, a fresh layout and a fresh workspace gives step 2 bit for bit as an
+    uninterrupted run."""
+    wl = inputs.WORKLOADS["ragged_small"]
+    W0, Gs, M0 = inputs.host_inputs(wl)
+    lay = capi.muon_layout_create(wl.shapes, 3, ns_dtype, wl.is_matrix)
+    ws = capi.workspace_tensor(lay)
+    W, M = split_shards(W0, 3), split_shards(M0, 3)
+    capi.muon_step(W, split_shards(Gs[0], 3), M, lay, ws, wl.lr, wl.wd, wl.mu, True, 5)
+    capi.muon_check()
+    W_saved, M_saved = join_shards(W, lay.numel), join_shards(M, lay.numel)
+    capi.muon_step(W, split_shards(Gs[1], 3), M, lay, ws, wl.lr, wl.wd, wl.mu, True, 5)
+    capi.muon_check()
+    lay2 = capi.muon_layout_create(wl.shapes, 3, ns_dtype, wl.is_matrix)
+    ws2 = capi.workspace_tensor(lay2)
+    W2, M2 = split_shards(W_saved, 3), split_shards(M_saved, 3)
+    capi.muon_step(W2, split_shards(Gs[1], 3), M2, lay2, ws2, wl.lr, wl.wd, wl.mu, True, 5)
+    capi.muon_check()
+    assert np.array_equal(join_shards(W2, lay.numel), join_shards(W, lay.numel))
+    assert np.array_equal(join_shards(M2, lay.numel), join_shards(M, lay.numel))
