@@ -111,6 +111,38 @@ def test_gather_scatter_bit_exact(capi, n_shards):
     assert np.array_equal(back, np.concatenate(want_sh).astype(np.float32))
 
 
+@pytest.mark.parametrize("n_shards,seed", [(2, 1), (7, 2), (128, 3)])
+def test_gather_scatter_random_layouts(capi, n_shards, seed):
+    """Gather and scatter bit-exact against the oracle's index maps on random shapes
+    (vectors mixed in, so matrices straddle shard edges at random places), up to the
+    largest shard count."""
+    rng = np.random.default_rng(seed)
+    shapes = [(int(rng.integers(1, 300)), int(rng.integers(1, 300))) for _ in range(12)]
+    is_matrix = [bool(rng.random() < 0.8) for _ in shapes]
+    lay = capi.muon_layout_create(shapes, n_shards, 0, is_matrix)
+    N = lay.numel
+    flat = rng.normal(size=N).astype(np.float32)
+    full = torch.full((max(1, lay.full_numel),), float("nan"), device="cuda")
+    capi.muon_gather_full(lay, split_shards(flat, n_shards), full)
+    torch.cuda.synchronize()
+    o = ref.flat_layout(shapes, n_shards, is_matrix)
+    want = ref.gather_full(ref.shard_flat(flat, o), o)
+    f = full.cpu().numpy()
+    for i, (r, c) in enumerate(shapes):
+        if is_matrix[i]:
+            off = lay.full_offsets[i]
+            assert np.array_equal(f[off: off + r * c].reshape(r, c), want[i].astype(np.float32)), i
+    y = {i: rng.normal(size=want[i].shape).astype(np.float32) for i in want}
+    sent = split_shards(np.full(N, 5.0, dtype=np.float32), n_shards)
+    for t in sent:
+        t.fill_(5.0)
+    capi.muon_scatter_updates(lay, mats_to_full(y, lay), sent)
+    torch.cuda.synchronize()
+    back = np.concatenate([t.cpu().numpy() for t in sent])
+    want_sh = ref.scatter_updates(y, o, [np.full(o["L"], 5.0) for _ in range(n_shards)])
+    assert np.array_equal(back, np.concatenate(want_sh).astype(np.float32))
+
+
 # ------------------------------------------------------------------ Newton-Schulz on given inputs
 def spectrum_inputs(wl, seed):
     rng = np.random.default_rng(seed)
