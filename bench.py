@@ -68,17 +68,23 @@ def elementwise_bytes(n_matrix_elems, ns_dtype):
 NS_TRAFFIC = {
     "llama3_8b_x32": {"bytes_per_launch": 16 * (22596132352 + 9347993344) / 15,
                       "tile_shape": 3,
-                      "sources_sha256": "e72b6d7349f27229bdb94e3e940d6ad46de3054e8f2e017ba155dc1b97f88d25"},
+                      "sources_sha256": "09e08220510768864a0b722a4f2e638be993760cf4d93d41053bd068f1e6ad8a"},
 }
 NS_SOURCES = ("gemm_ns.cu", "device_common.cuh", "layout.cpp")
 
 
 def _ns_sources_sha256():
+    """Digest of the kernel sources' code: comments and whitespace are dropped, so that a
+    change of wording alone keeps the measured traffic."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in NS_SOURCES:
-        with open(os.path.join(ROOT, "muon_optimizer_step_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "muon_optimizer_step_gb300", "csrc", f)) as fh:
+            code = fh.read()
+        code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
+        code = re.sub(r"//[^\n]*", " ", code)
+        h.update(" ".join(code.split()).encode())
     return h.hexdigest()
 
 

@@ -4,8 +4,9 @@
  *
  * Sources (page title, section):
  *   [P1] "Add initial Muon+M-FSDPv2 implementation" (Megatron-LM pull request #6425):
- *        "What does this PR do?" (all-Flat placements; owner-based design; non-matrix
- *        parameters computed as usual) and the "Opt step" pseudocode, steps 1-6.
+ *        "What does this PR do?" (every parameter placed in flat shards; one owner rank
+ *        orthogonalizes each sharded matrix; other parameters take the regular optimizer
+ *        path) and the "Opt step" pseudocode, steps 1-6.
  *   [P2] "core.distributed.fsdp.src.megatron_fsdp.experimental.muon" (Megatron-Core
  *        API docs), class FsdpMuon: step(), _step_group(), _compute_momentum_inputs(),
  *        _orthogonalize_updates(), _apply_local_updates(), "Limitations".
@@ -73,7 +74,7 @@ typedef enum muon_ns_dtype {
 typedef struct muon_layout muon_layout; /* opaque */
 
 /* ---------------------------------------------------------------- layout (host only)
- * muon_layout_create: describe one flat buffer ([P1] "all-Flat placements";
+ * muon_layout_create: describe one flat buffer ([P1]: every parameter in flat shards;
  * [P2] FsdpMuon, one FSDP buffer = one parameter group).
  *   shapes     n_params (rows, cols) pairs, int64, in flat-buffer order.  Parameters are
  *              packed back to back with no padding; N = sum(rows*cols).
@@ -179,7 +180,7 @@ muon_status muon_orthogonalize_apply(float* const* flat_params, const muon_layou
  * muon_assign_owners plans this for a data-parallel group of n_shards ranks (rank r holds
  * shard r): matrices in decreasing Newton-Schulz cost 5*(3 m^2 n + m^3)*ns_steps/5, each to
  * the least-loaded rank among those holding a part of it (ties: lowest rank), so a matrix
- * inside one shard stays on its rank ("computed fully locally").  owner: host array of
+ * inside one shard stays on the rank that holds it.  owner: host array of
  * n_params entries (-1 for non-matrix parameters); rank_cost: host array of n_shards flop
  * totals, or NULL.  Pure host work, deterministic, so every rank computes the same plan. */
 muon_status muon_assign_owners(const muon_layout* layout, int32_t ns_steps, int32_t* owner,

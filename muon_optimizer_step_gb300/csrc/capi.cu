@@ -1,8 +1,8 @@
 // C ABI of libmuon.so: argument validation, device tables, and the launch sequence of the
 // Muon step.  The step follows FsdpMuon._step_group of the Megatron-Core API docs
-// ("core.distributed.fsdp.src.megatron_fsdp.experimental.muon"): compute momentum
-// inputs, orthogonalize on the owner, apply local updates, one flat buffer at a time on
-// the caller's CUDA stream.  With one GPU the owner is this device and the gather /
+// ("core.distributed.fsdp.src.megatron_fsdp.experimental.muon"): its three stages
+// (momentum inputs, orthogonalization on the owner, local apply) run for one flat
+// buffer per call, enqueued on the stream the caller passes.  With one GPU the owner is this device and the gather /
 // scatter of "Add initial Muon+M-FSDPv2 implementation" ("Opt step" steps 3 and 5) are
 // index maps fused into the first and last kernels.
 #include <cmath>

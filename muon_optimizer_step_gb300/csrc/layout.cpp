@@ -3,7 +3,7 @@
 // and the per-phase tile work lists of the Newton-Schulz GEMMs.
 //
 // Flat packing follows "Add initial Muon+M-FSDPv2 implementation" ("What does this PR
-// do?": all-Flat placements): parameters back to back in the caller's order, no padding,
+// do?": every parameter in flat shards): parameters back to back in the caller's order, no padding,
 // shard s of n_shards holding flat [s*L, (s+1)*L) with L = ceil(N / n_shards).  Matrix
 // parameters may straddle any number of shard edges; the gather and scatter of the
 // owner ("Opt step" steps 3 and 5) are then the index map built here.

@@ -7,13 +7,14 @@ module; only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 Sources, by page and section:
 
 * "Add initial Muon+M-FSDPv2 implementation" (Megatron-LM pull request #6425),
-  section "What does this PR do?" (all-Flat placements, owner-based design, non-matrix
-  parameters left to the usual optimizer) and its "Opt step" pseudocode, steps 1-6.
+  section "What does this PR do?" (every parameter placed in flat shards; one owner
+  rank orthogonalizes each sharded matrix; parameters that are not matrices take the
+  regular optimizer path) and its "Opt step" pseudocode, steps 1-6.
 * "core.distributed.fsdp.src.megatron_fsdp.experimental.muon" (Megatron-Core API
-  docs), class ``FsdpMuon``: ``_compute_momentum_inputs`` ("apply local weight decay,
-  update momentum, and build inputs for orthogonalization"),
-  ``_orthogonalize_updates`` and ``_apply_local_updates``; "Limitations" (non-2-D
-  parameters are skipped).
+  docs), class ``FsdpMuon``: ``_compute_momentum_inputs`` (its first stage: the
+  decoupled weight decay, the momentum update and the orthogonalization input),
+  ``_orthogonalize_updates`` and ``_apply_local_updates``; "Limitations" (only 2-D
+  parameters take the Muon update).
 
 The pages hand the Muon arithmetic to the base class (emerging_optimizers' Muon) and do
 not print it.  This oracle takes the standard reading of that base class:
@@ -27,7 +28,7 @@ not print it.  This oracle takes the standard reading of that base class:
 * decoupled weight decay W <- W*(1 - lr*wd) in the first stage (as
   ``_compute_momentum_inputs`` lists it), then W <- W - lr*sqrt(max(1, rows/cols))*O.
 
-Flat layout (the pages say "all-Flat placements" without fixing padding): parameters
+Flat layout (the pages place every parameter in flat shards but fix no padding): parameters
 packed back to back in the given order with no padding, N elements in all; with S
 shards each shard holds L = ceil(N/S) elements, shard s covering flat [s*L, (s+1)*L);
 the tail of the last shard is padding and is never touched.
