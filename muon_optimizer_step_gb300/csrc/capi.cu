@@ -174,12 +174,13 @@ muon_status ensure_device(muon_layout* L) {
     const bool cluster = shape != kShapeSingle;
     t.tc_shape = shape;
     t.tc_units = cluster ? pairs : singles;
-    // One persistent launch when a phase carries little work (< 100 GFLOP, e.g. the
-    // GPT-2-small set: 8% faster there); a launch per phase otherwise (Llama-3-8B: twice as
-    // fast as persistent; MoE: 16% faster), where each phase's tiles are balanced alone.
-    // The split-fp32 epilogue writes with plain stores, which the persistent launch's
-    // counters do not publish to the next phase's TMA reads: one launch per phase there.
-    t.tc_persistent = !split && all / 3.0 < 100e9;
+    // One launch per phase, each phase's tiles balanced on their own.  The persistent
+    // launch (every phase in one launch, tiles waiting on per-matrix counters) measured
+    // slower on every set: GPT-2-small 2.15 against 2.10 ms, MoE 20.5 against 16.6 ms,
+    // Llama-3-8B about twice as long; it stays available for measurements.  The split-fp32
+    // epilogue writes with plain stores, which the persistent launch's counters do not
+    // publish to the next phase's TMA reads, so it never runs persistent.
+    t.tc_persistent = false;
     const char* pv = split ? nullptr : std::getenv("MUON_NS_PERSISTENT");  // "1"/"0" pins it
     if (pv != nullptr && (pv[0] == '0' || pv[0] == '1')) t.tc_persistent = pv[0] == '1';
     for (MatDev& m : L->plan.mats) m.sig[0] = m.sig[1] = m.sig[2] = 0;

@@ -1,6 +1,6 @@
 // bf16 Newton-Schulz on the sm_103a tensor cores (tcgen05 + TMEM + TMA): the phases of
-// every matrix of a flat buffer as grouped launches, one per phase, or all of them in one
-// persistent, cooperative launch (small buffers).
+// every matrix of a flat buffer as grouped launches, one per phase, or (when pinned) all
+// of them in one persistent, cooperative launch.
 //
 // Phases of one iteration (quintic Newton-Schulz, (a, b, c) = (3.4445, -4.7750, 2.0315)):
 //   Gram    A = X X^T           (tall X: A = X^T X)      upper-triangle tiles, mirrored

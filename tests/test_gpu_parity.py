@@ -480,10 +480,9 @@ def test_smoke_entry_point(capi):
 
 
 def test_default_kernel_choice(capi, monkeypatch):
-    """CTA pairs with a launch per phase for two Llama-3-8B layers; 2-CTA clusters with
-    multicast B for the 32-layer set (94 TFLOP per iteration: long enough to run at the
-    power limit); CTA pairs in one persistent launch for the GPT-2-small set; nothing on
-    the fp32 path."""
+    """CTA pairs for two Llama-3-8B layers and for the GPT-2-small set; 2-CTA clusters
+    with multicast B for the 32-layer set (94 TFLOP per iteration: long enough to run at
+    the power limit); one launch per phase everywhere; nothing on the fp32 path."""
     monkeypatch.delenv("MUON_TC_KERNEL", raising=False)
     monkeypatch.delenv("MUON_NS_PERSISTENT", raising=False)
 
@@ -496,7 +495,7 @@ def test_default_kernel_choice(capi, monkeypatch):
     k = choice("llama3_8b_x32")
     assert k["tile_shape"] == 3 and not k["persistent"] and k["units"] >= 1, k
     k = choice("gpt2_small_x12")
-    assert k["tile_shape"] == 2 and k["persistent"] and k["units"] >= 1, k
+    assert k["tile_shape"] == 2 and not k["persistent"] and k["units"] >= 1, k
     assert choice("gpt2_small_x12", 1) == {"tile_shape": 0, "units": 0, "persistent": False}
 
 
