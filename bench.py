@@ -36,9 +36,9 @@ DEFAULT_WORKLOAD = "llama3_8b_x32"
 def ns_flops(shapes, is_matrix, ns_steps):
     """(symmetric, dense) Newton-Schulz flop counts of one step.
 
-    Per iteration and matrix (m = min, n = max of the shape): the Gram X X^T costs m^2 n
-    multiply-adds on its upper half, A A costs m^3 / 2 on its upper half, B X costs m^2 n:
-    2 flops per multiply-add gives 3 m^2 n + m^3 (symmetric) against 4 m^2 n + 2 m^3 (dense).
+    Per iteration and matrix (m = min, n = max of the shape), in multiply-adds: the Gram
+    X X^T on its upper half m^2 n / 2, A A on its upper half m^3 / 2, B X m^2 n; 2 flops per
+    multiply-add gives 3 m^2 n + m^3 (symmetric) against 4 m^2 n + 2 m^3 (dense).
     """
     sym = dense = 0.0
     for (r, c), f in zip(shapes, is_matrix):

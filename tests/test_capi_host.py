@@ -128,3 +128,19 @@ def test_set_groups_validation_on_host():
         capi.muon_layout_set_groups(lay, [0, 0], 33)
     with pytest.raises(capi.MuonError):
         capi.muon_layout_set_groups(lay, [0, 0], 0)
+
+
+def test_header_constants_match_the_binding():
+    """Every enum value and #define of the C header has the same value in the binding."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    consts = {}
+    for name, val in re.findall(r"\b(MUON_[A-Z0-9_]+)\s*=\s*(\d+)", text):
+        consts[name] = int(val)
+    for name, val in re.findall(r"#define\s+(MUON_[A-Z0-9_]+)\s+(\d+)", text):
+        consts[name] = int(val)
+    assert {"MUON_OK", "MUON_ERR_UNSUPPORTED", "MUON_NS_SPLIT_FP32", "MUON_MAX_SHARDS"} <= set(consts)
+    for name, val in consts.items():
+        if name == "MUON_ABI_VERSION":
+            assert capi.muon_abi_version() == val
+        else:
+            assert getattr(capi, name) == val, name

@@ -149,3 +149,21 @@ def test_surviving_rank_gets_an_error_when_a_rank_dies(tmp_path):
     assert float(elapsed) < 3 * timeout_s
     import bench
     assert 60 <= bench.PG_TIMEOUT_S <= 3600
+
+
+def test_bench_flop_and_byte_models():
+    """bench.py's roofline arithmetic: symmetric and dense Newton-Schulz flop counts of a
+    single matrix (tall and wide give the same count), the streaming byte model, and the
+    traffic record's code digest ignoring comments."""
+    import bench
+    sym, dense = bench.ns_flops([(256, 128)], [True], 5)
+    m, n = 128, 256
+    assert sym == 5 * (3 * m * m * n + m ** 3)
+    assert dense == 5 * (4 * m * m * n + 2 * m ** 3)
+    assert bench.ns_flops([(128, 256)], [True], 5) == (sym, dense)
+    assert bench.ns_flops([(128, 256)], [False], 5) == (0, 0)
+    assert bench.elementwise_bytes(10, "bf16") == (140, 100)
+    assert bench.elementwise_bytes(10, "fp32") == (160, 120)
+    assert bench.elementwise_bytes(10, "split") == (180, 140)
+    d = bench._ns_sources_sha256()
+    assert len(d) == 64 and d == bench._ns_sources_sha256()
