@@ -796,6 +796,12 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
             const int r0 = tile.i0 + (kCluster ? 128 * (int)rank : 0) + 32 * q;
             const int i = r0 + lane;
             const int c_first = half * (BN / 64), c_last = (half + 1) * (BN / 64);
+            // The X (Update) or A (Poly) input of the next 32 x 32 block is loaded before
+            // this block's TMEM load and math, so that its memory latency overlaps them.
+            uint4 in_next[4];
+            bool have_next = false;
+            if constexpr (kVar == kVarTma)
+              have_next = epilogue_prefetch(p, mt, phase, x_in, i, tile.j0 + 32 * c_first, in_next);
 #pragma unroll 1
             for (int c = c_first; c < c_last; ++c) {
               uint32_t v[32];
@@ -807,8 +813,12 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
                                                lane, v, s);
               } else {
                 uint4 in_cur[4];
-                const bool have_cur = epilogue_prefetch(p, mt, phase, x_in, i, tile.j0 + 32 * c,
-                                                        in_cur);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) in_cur[k] = in_next[k];
+                const bool have_cur = have_next;
+                if (c + 1 < c_last)
+                  have_next = epilogue_prefetch(p, mt, phase, x_in, i, tile.j0 + 32 * (c + 1),
+                                                in_next);
                 tmem_ld_32x32b_x32(
                     tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * BN + 32 * c), v);
                 tmem_ld_wait();
