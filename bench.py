@@ -290,6 +290,15 @@ def _mem_available_bytes():
     return 0
 
 
+def host_memory_allows(need_bytes, world, dist, device, available=None):
+    """Whether every rank may pin `need_bytes` of host memory.  The ranks share one host:
+    each asks for room for all of them (three times the total, for headroom), and all
+    skip together when any rank sees too little."""
+    avail = _mem_available_bytes() if available is None else available
+    short = 0.0 if avail > 3 * need_bytes * world else 1.0
+    return reduce_max_over_ranks([short], dist, device)[0] == 0.0
+
+
 def _pin_to_gpu_numa_node(dev):
     """Run this thread on the CPUs next to the GPU, so pinned pages land on its node."""
     try:
@@ -415,7 +424,8 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         need = 2 * 4 * N
-        if _mem_available_bytes() > 3 * need:
+        barrier()
+        if host_memory_allows(need, world, dist, dev):
             saved_affinity = os.sched_getaffinity(0)
             _pin_to_gpu_numa_node(dev)
             G_h = torch.empty(N, dtype=torch.float32, pin_memory=True)
@@ -476,7 +486,8 @@ def run_ours(args):
         else:
             e2e = {"value": None, "unit": "ms", "h2d_bytes_per_step": 4 * N,
                    "d2h_bytes_per_step": 4 * N,
-                   "note": "not measured: not enough host memory for pinned buffers"}
+                   "note": "not measured: not enough host memory to pin %.1f GB per rank "
+                           "for %d rank(s)" % (need / 1e9, world)}
 
     if rank != 0:
         if dist is not None:

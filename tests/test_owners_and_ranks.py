@@ -167,3 +167,36 @@ def test_bench_flop_and_byte_models():
     assert bench.elementwise_bytes(10, "split") == (180, 140)
     d = bench._ns_sources_sha256()
     assert len(d) == 64 and d == bench._ns_sources_sha256()
+
+
+def _rank_mem_main(rank, world, port, out_dir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    need = 10 ** 9
+    both = bench.host_memory_allows(need, world, dist, "cpu", available=100 * need)
+    # one rank sees too little: nobody pins
+    one = bench.host_memory_allows(need, world, dist, "cpu",
+                                   available=100 * need if rank == 0 else 5 * need)
+    # room for one rank's buffers but not for both
+    tight = bench.host_memory_allows(need, world, dist, "cpu", available=4 * need)
+    with open(os.path.join(out_dir, f"mem{rank}.txt"), "w") as f:
+        f.write(f"{int(both)} {int(one)} {int(tight)}\n")
+    dist.destroy_process_group()
+
+
+def test_ranks_agree_on_pinning_host_memory(tmp_path):
+    """The e2e measurement pins host memory on every rank of one host: the ranks decide
+    together, with room for all of them, so that N ranks cannot exhaust the host."""
+    import torch.multiprocessing as mp
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    mp.start_processes(_rank_mem_main, args=(2, port, str(tmp_path)), nprocs=2,
+                       start_method="spawn")
+    for r in range(2):
+        assert open(tmp_path / f"mem{r}.txt").read().split() == ["1", "0", "0"]
