@@ -27,6 +27,10 @@ namespace {
 
 thread_local std::string g_last_error;
 constexpr long long kDefaultBudget = 4000000000LL;  // ~2 s of SM clock per wait
+// Newton-Schulz work of one iteration (flops, symmetric count) from which a buffer counts
+// as a long step that runs at the power limit, and the tile shape such buffers get.
+constexpr double kLongStepFlops = 20e12;
+constexpr int kLongStepShape = kShapeSingle;
 constexpr int kMaxDevices = 64;
 int* g_err_word[kMaxDevices] = {nullptr};
 std::mutex g_err_mu;
@@ -138,21 +142,20 @@ muon_status ensure_device(muon_layout* L) {
       free_tables(&t);
       return fail(MUON_ERR_UNSUPPORTED, "the tcgen05 kernel does not fit on an SM of device %d", dev);
     }
-    // Three tile shapes, measured on GB300 (bench, bf16):
+    // Two tile shapes, measured on GB300 (bench, bf16):
     //  - CTA pairs (cta_group::2, 256 x 256 tiles) keep the tensor pipe busiest per clock
     //    (74-76% of active cycles against 71% for single CTAs on two Llama-3-8B layers) and
     //    are 2-6% faster wherever the clock stays high: GPT-2, MoE, two Llama layers.
     //  - Steps long enough to hold the GPU at its 1.4 kW limit (the 32-layer Llama-3-8B
-    //    set) are decided by energy per flop instead.  There 2-CTA clusters that multicast
-    //    the shared B operand (each CTA on cta_group::1) clock highest (~1800 MHz against
-    //    ~1740 single, ~1600 pairs) and finish first: 356 ms against 359 and 361.
+    //    set) are decided by energy per flop instead; there single CTAs hold a higher clock
+    //    than pairs (~1740 against ~1600 MHz) and finish first.
     // The cut between the two regimes is the Newton-Schulz work of one iteration: 94 TFLOP
     // on the 32-layer set, 6 on the two-layer one.
     double all = 0.0;  // flops of one iteration, symmetric count: 3 m^2 n + m^3 per matrix
     for (const MatDev& m : L->plan.mats)
       all += 3.0 * m.m * (double)m.m * m.n + (double)m.m * m.m * m.m;
-    int shape = pairs < 1 ? kShapeSingle : (all < 20e12 ? kShapePair : kShapeMcast);
-    const char* v = split ? nullptr : std::getenv("MUON_TC_KERNEL");  // "1"-"3" pins a shape
+    int shape = pairs < 1 ? kShapeSingle : (all < kLongStepFlops ? kShapePair : kLongStepShape);
+    const char* v = split ? nullptr : std::getenv("MUON_TC_KERNEL");  // "1" or "2" pins a shape
     if (split) {
       // The split-fp32 kernel exists for CTA pairs only (two 96 KB operand stages).
       if (pairs < 1) {
@@ -162,7 +165,12 @@ muon_status ensure_device(muon_layout* L) {
       }
       shape = kShapePair;
     }
-    if (v != nullptr && v[0] >= '1' && v[0] <= '3') {
+    if (v != nullptr && v[0] != '\0') {
+      if ((v[0] != '1' && v[0] != '2') || v[1] != '\0') {
+        free_tables(&t);
+        return fail(MUON_ERR_INVALID_ARG, "MUON_TC_KERNEL=%s: the tile shapes are 1 (single "
+                    "CTA) and 2 (CTA pair)", v);
+      }
       shape = v[0] - '0';
       if (shape != kShapeSingle && pairs < 1) {
         free_tables(&t);

@@ -260,26 +260,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const void* 
       : "memory");
 }
 
-// TMA load multicast to the CTAs of `mask` in this cluster: each receives the box at the
-// same shared-memory offset, and the mbarrier at the same offset in each gets the bytes.
-__device__ __forceinline__ void tma_load_2d_mcast(uint32_t smem_dst, const void* tmap, int x, int y,
-                                                  uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_dst),
-      "l"(tmap), "r"(x), "r"(y), "r"(bar), "h"(mask)
-      : "memory");
-}
-
-// Arrives (once each) on the mbarrier at this offset in every CTA of `mask` when this
-// CTA's MMAs issued so far complete.
-__device__ __forceinline__ void tc_commit_mcast(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* smem_slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    smem_u32(smem_slot)),

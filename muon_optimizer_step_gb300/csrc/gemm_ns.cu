@@ -74,8 +74,7 @@ struct Cfg {
   static constexpr int MMA_M = kTwoSm ? 256 : 128;    // rows of one MMA instruction
   static constexpr int BROWS = kCluster ? 128 : 256;  // B-operand rows this CTA loads
   static constexpr int A_PART = 128 * 128;            // 16 KB: 128 rows of 128 bytes
-  // B rows held in this CTA's stage: its own half (pair), or all 256 (single; multicast,
-  // where the peer CTA's half arrives by multicast)
+  // B rows held in this CTA's stage: its own half (pair), or all 256 (single)
   static constexpr int B_PART = (kTwoSm ? 128 : 256) * 128;
   static constexpr int A_BYTES = A_PART * PARTS;
   static constexpr int B_BYTES = B_PART * PARTS;
@@ -519,8 +518,7 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);   // the (pair: even) CTA's arrival with the expected bytes
-      // the MMA commit; with multicast B, both CTAs' commits (the peer's copies land here)
-      mbar_init(&empty[s], kShape == kShapeMcast ? 2 : 1);
+      mbar_init(&empty[s], 1);  // the MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -619,20 +617,7 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
                 } else {
                   tma_load_2d(sa, amap, k0, ia, &full[stage]);
                 }
-                if (kShape == kShapeMcast) {
-                  // This CTA's half of B goes to both CTAs' stages, at the half's offset;
-                  // each CTA's full barrier counts both halves.
-                  const uint32_t sbh = smem_u32(sb) + rank * (uint32_t)(C::B_BYTES / 2);
-                  const uint32_t fb = smem_u32(&full[stage]);
-                  if (ops.b_mn) {
-#pragma unroll
-                    for (int q = 0; q < C::BROWS / C::MN_W; ++q)
-                      tma_load_2d_mcast(sbh + q * C::MN_BOX, bmap, jr + C::MN_W * q, k0, fb,
-                                        (uint16_t)0x3);
-                  } else {
-                    tma_load_2d_mcast(sbh, bmap, k0, jr, fb, (uint16_t)0x3);
-                  }
-                } else if (ops.b_mn) {
+                if (ops.b_mn) {
 #pragma unroll
                   for (int q = 0; q < C::BROWS / C::MN_W; ++q)
                     tma_load_2d(sb + q * C::MN_BOX, bmap, jr + C::MN_W * q, k0, &full[stage]);
@@ -650,8 +635,7 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
         }
       }
       // Every copy issued must land before the block exits (already true unless aborted).
-      // For a pair the even CTA's full barriers count both CTAs' copies; with multicast B
-      // each CTA's count the peer's copies into it.
+      // For a pair the even CTA's full barriers count both CTAs' copies.
       if (mma_cta)
         for (long long k = nfill - 1; k >= 0 && k >= nfill - C::STAGES; --k)
           wait_drain(&full[k % C::STAGES], (uint32_t)((k / C::STAGES) & 1), p.budget, p.err);
@@ -672,15 +656,11 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
             const TileDev tile = p.tiles[phase][ti];
             const MatDev& mt = p.mats[tile.mat];
             const TileOps ops = tile_ops<kCluster>(mt, phase, it & 1);
-            // Columns the epilogue would discard are not computed (CTAs that issue their
-            // own MMAs, i.e. all but CTA pairs):
-            //  - symmetric phases: a CTA whose rows all lie at or below the tile's second
-            //    column half (single CTAs with i0 = j0 + 128; the odd CTA of a multicast
-            //    cluster on a diagonal tile) skips the first half;
-            //  - a tile whose second column half lies outside the matrix skips that half;
-            //  - a CTA whose rows all lie outside the matrix (the odd CTA of a multicast
-            //    cluster on a ragged last row band) issues no MMAs, only the commits that
-            //    hand its stages back.
+            // Columns the epilogue would discard are not computed (single CTAs; a pair's
+            // MMA covers both CTAs' rows, so it cannot skip per CTA):
+            //  - symmetric phases: a tile whose rows all lie at or below its second column
+            //    half (i0 = j0 + 128) skips the first half;
+            //  - a tile whose second column half lies outside the matrix skips that half.
             // A half is done as N = 128 MMAs on that half of B, into that half of the
             // accumulator.
             const int row0 = tile.i0 + (kCluster ? 128 * (int)rank : 0);
@@ -740,7 +720,6 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
                 }
               }
               if (kTwoSm) tc_commit_pair(&empty[stage], (uint16_t)0x3);
-              else if (kShape == kShapeMcast) tc_commit_mcast(&empty[stage], (uint16_t)0x3);
               else tc_commit(&empty[stage]);
               if (++stage == C::STAGES) {
                 stage = 0;
@@ -881,11 +860,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   ns_tc_body<kShapePair>(p);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    ns_tc_mcast_kernel(const __grid_constant__ NsParams p) {
-  ns_tc_body<kShapeMcast>(p);
-}
-
 // The split-fp32 form, on CTA pairs.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     ns_tc_split_kernel(const __grid_constant__ NsParams p) {
@@ -896,8 +870,7 @@ using NsKernel = void (*)(NsParams);
 
 template <int kShape>
 NsKernel ns_tc_kernel_of() {
-  return kShape == kShapeSingle ? ns_tc_single_kernel
-                                : (kShape == kShapePair ? ns_tc_pair_kernel : ns_tc_mcast_kernel);
+  return kShape == kShapeSingle ? ns_tc_single_kernel : ns_tc_pair_kernel;
 }
 
 __global__ void selftest_timeout_kernel(int* err, long long budget) {
@@ -964,11 +937,11 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
 }  // namespace
 
 cudaError_t prepare_ns_kernels(int* max_pairs, int* max_singles) {
-  const void* fns[4] = {(const void*)ns_tc_single_kernel, (const void*)ns_tc_pair_kernel,
-                        (const void*)ns_tc_mcast_kernel, (const void*)ns_tc_split_kernel};
-  const int smems[4] = {Cfg<kShapeSingle>::SMEM_BYTES, Cfg<kShapePair>::SMEM_BYTES,
-                        Cfg<kShapeMcast>::SMEM_BYTES, Cfg<kShapePair, kVarSplit>::SMEM_BYTES};
-  for (int k = 0; k < 4; ++k) {
+  const void* fns[3] = {(const void*)ns_tc_single_kernel, (const void*)ns_tc_pair_kernel,
+                        (const void*)ns_tc_split_kernel};
+  const int smems[3] = {Cfg<kShapeSingle>::SMEM_BYTES, Cfg<kShapePair>::SMEM_BYTES,
+                        Cfg<kShapePair, kVarSplit>::SMEM_BYTES};
+  for (int k = 0; k < 3; ++k) {
     const void* fn = fns[k];
     const int smem = smems[k];
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -986,15 +959,13 @@ cudaError_t prepare_ns_kernels(int* max_pairs, int* max_singles) {
   *max_singles = per_sm * sms;
   // Resident 2-CTA clusters: the smallest count of the cluster kernels.
   int n_min = 1 << 30;
-  for (int k = 1; k < 4; ++k) {
+  for (int k = 1; k < 3; ++k) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * 1024, 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smems[k];
     int n = 0;
-    const NsKernel kern = k == 1 ? ns_tc_pair_kernel
-                          : k == 2 ? ns_tc_mcast_kernel
-                                   : ns_tc_split_kernel;
+    const NsKernel kern = k == 1 ? ns_tc_pair_kernel : ns_tc_split_kernel;
     e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
     if (e != cudaSuccess) return e;
     n_min = n < n_min ? n : n_min;
@@ -1016,8 +987,6 @@ cudaError_t launch_ns_tc(const Plan& plan, const DevTables& dt, void* ws, int ns
             ? launch_impl<kShapePair, kVarSplit>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
         : dt.tc_shape == kShapePair
             ? launch_impl<kShapePair>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
-        : dt.tc_shape == kShapeMcast
-            ? launch_impl<kShapeMcast>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
             : launch_impl<kShapeSingle>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st);
     if (e != cudaSuccess) return e;
   }

@@ -18,8 +18,6 @@ struct GroupParams;
 // muon_layout_ns_kernel reports).
 constexpr int kShapeSingle = 1;  // one CTA per 128 x 256 tile, tcgen05 cta_group::1
 constexpr int kShapePair = 2;    // 2-CTA cluster per 256 x 256 tile, tcgen05 cta_group::2
-constexpr int kShapeMcast = 3;   // 2-CTA cluster per 256 x 256 tile, each CTA cta_group::1
-                                 // on its 128 rows, the B operand multicast to both
 
 // Device-resident tables of a layout (uploaded once per device).
 struct DevTables {
