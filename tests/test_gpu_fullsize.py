@@ -4,9 +4,11 @@ straddling parameters (bf16, fp32 and split-fp32 Newton-Schulz).
 
 The oracle cannot run the whole step, so the checks are (a) bit-exact gather / scatter
 over every element, (b) momentum and weights on a seeded sample of a million flat
-positions, computed one by one in fp64, and (c) Newton-Schulz on sampled matrices of
-each kind (wide k/v, square q/o, tall gate/up), run by the oracle on the GPU's own
-stored input.
+positions, computed one by one in fp64 and bounded element by element, and (c)
+Newton-Schulz on sampled matrices of each kind (wide k/v, square q/o, tall gate/up, wide
+down), run by the oracle on the GPU's own stored input and bounded whole, per 128 x 128
+tile and per element (tests/parity.py).  One test runs muon_step itself, the fused path
+bench.py times, with the default kernel choice.
 """
 import numpy as np
 import pytest
@@ -16,6 +18,7 @@ pytestmark = pytest.mark.gpu
 
 from oracle import muon_ref as ref  # noqa: E402
 from muon_optimizer_step_gb300 import inputs  # noqa: E402
+from tests import parity  # noqa: E402
 
 TOL_NS = {0: 2e-2, 1: 1e-4, 2: 1e-4}
 TOL_STATE = 1e-6
@@ -103,6 +106,7 @@ def run_full(capi, wl_name, ns_dtype, sample_params):
     # momentum on the sample (M0 = 0): M1 = G
     M_s = Mb[idx].double().cpu().numpy()
     assert rel(M_s, ref.momentum_update(np.zeros_like(G_s), G_s, wl.mu)) < TOL_STATE
+    parity.check_momentum(M_s, ref.momentum_update(np.zeros_like(G_s), G_s, wl.mu), 0.0, "sample")
     # weights on the sample, given the GPU's own O
     flat_to_full = np.zeros(len(wl.shapes), dtype=np.int64)
     for i in range(len(wl.shapes)):
@@ -112,21 +116,25 @@ def run_full(capi, wl_name, ns_dtype, sample_params):
     O_s = full[torch.from_numpy(idx.cpu().numpy() + flat_to_full[owner]).cuda()].double().cpu().numpy()
     scale = np.array([ref.update_scale(*wl.shapes[k]) for k in owner])
     want_w = ref.weight_decay(W_prev, wl.lr, wl.wd) - wl.lr * scale * O_s
-    assert rel(Wb[idx].double().cpu().numpy(), want_w) < TOL_STATE
+    W_s = Wb[idx].double().cpu().numpy()
+    assert rel(W_s, want_w) < TOL_STATE
+    parity.check_weights(W_s, want_w, W_prev, 1 - wl.lr * wl.wd, wl.lr * scale * O_s, what="sample")
     # Newton-Schulz on sampled matrices, oracle on the GPU's stored input
     for i in sample_params:
         r, c = wl.shapes[i]
         off = lay.full_offsets[i]
         O = full[off: off + r * c].view(r, c).double().cpu().numpy()
-        e = rel(O, ref.newton_schulz(X_in[i], wl.ns_steps))
-        assert e < TOL_NS[ns_dtype], (i, (r, c), e)
+        rep = parity.check_ns(O, ref.newton_schulz(X_in[i], wl.ns_steps), ns_dtype, (i, (r, c)))
+        print("NS", wl_name, ns_dtype, i, (r, c), rep)
     del Wb, Gb, Mb, W, G, M, ws, full
     torch.cuda.empty_cache()
 
 
 def test_llama_full_size_bf16(capi):
-    # layer 0 k (wide 1024x4096), layer 5 q (square), layer 31 gate (tall 14336x4096)
-    run_full(capi, "llama3_8b_x32", 0, [0 * LAYER + 2, 5 * LAYER + 0, 31 * LAYER + 4])
+    # layer 0 k (wide 1024x4096), layer 5 q (square), layer 31 gate (tall 14336x4096),
+    # layer 17 down (wide 4096x14336)
+    run_full(capi, "llama3_8b_x32", 0, [0 * LAYER + 2, 5 * LAYER + 0, 31 * LAYER + 4,
+                                        17 * LAYER + 6])
 
 
 def test_llama_8_shards_straddling_bf16(capi):
@@ -142,3 +150,62 @@ def test_llama_8_shards_split_fp32_ns(capi):
     # layer 2's gate (tall: MN-major Gram operands), layer 3's down projection (wide,
     # straddling shards 0 and 1: MN-major Update operand)
     run_full(capi, "llama3_8b_8shards", 2, [1 + 2 * LAYER + 4, 1 + 3 * LAYER + 6])
+
+
+def test_llama_full_size_muon_step_fused(capi):
+    """muon_step itself on the 32-layer set: the default kernel choice (as bench.py runs
+    it), momentum and inputs on the GPU, Newton-Schulz, and the last Update applying W in
+    its epilogue.  Checked:
+      * momentum on a million sampled positions (M0 = 0, so M1 = G exactly);
+      * the update O (the bf16 values the last Update stores) of one matrix of every shape
+        against the oracle's Newton-Schulz of the GPU's own input, which is rebuilt on the
+        host bit for bit: X = bf16(fp32(0.95f * G + G)) (with M0 = 0 the Nesterov input
+        is one fp32 fused multiply-add of G, then rounded to bf16);
+      * W on the sample against the oracle's decay and apply of that O, within the bf16
+        rounding of O (the fused tail applies the fp32 value before rounding it):
+        lr * s * 2^-8 * |O| per element, plus the fp32 floor."""
+    wl = inputs.WORKLOADS["llama3_8b_x32"]
+    lay = capi.muon_layout_create(wl.shapes, 1, 0, wl.is_matrix)
+    k = capi.muon_layout_ns_kernel(lay)
+    N = lay.numel
+    W = torch.zeros(N, device="cuda")
+    G = torch.zeros(N, device="cuda")
+    M = torch.zeros(N, device="cuda")
+    inputs.device_fill_weights(wl, W)
+    inputs.device_fill_grads(wl, G, 0)
+    ws = capi.workspace_tensor(lay)
+    rng = np.random.default_rng(321)
+    idx = torch.from_numpy(rng.integers(0, N, 1_000_000)).cuda()
+    W_prev = W[idx].double().cpu().numpy()
+    pick = [0 * LAYER + 0, 3 * LAYER + 3, 30 * LAYER + 5, 31 * LAYER + 6]  # q, v, up, down
+    offs = np.concatenate([[0], np.cumsum([r * c for r, c in wl.shapes])])
+    G_m = {i: G[offs[i]: offs[i + 1]].cpu().numpy() for i in pick}
+    torch.cuda.synchronize()
+    capi.muon_step([W], [G], [M], lay, ws, wl.lr, wl.wd, wl.mu, wl.nesterov, wl.ns_steps)
+    full = torch.empty(lay.full_numel, device="cuda")
+    capi.muon_export_update(lay, ws, wl.ns_steps, full)
+    capi.muon_check()
+    G_s = G[idx].double().cpu().numpy()
+    parity.check_momentum(M[idx].double().cpu().numpy(),
+                          ref.momentum_update(np.zeros_like(G_s), G_s, wl.mu), 0.0, "sample")
+    del M
+    # every sampled position lies in some matrix (the set has no vectors)
+    owner = np.searchsorted(offs[1:], idx.cpu().numpy(), side="right")
+    pos_full = np.array(lay.full_offsets)[owner] + (idx.cpu().numpy() - offs[owner])
+    O_s = full[torch.from_numpy(pos_full).cuda()].double().cpu().numpy()
+    scale = np.array([ref.update_scale(*wl.shapes[j]) for j in owner])
+    want_w = ref.weight_decay(W_prev, wl.lr, wl.wd) - wl.lr * scale * O_s
+    lrs_o = wl.lr * scale * O_s
+    parity.check_weights(W[idx].double().cpu().numpy(), want_w, W_prev, 1 - wl.lr * wl.wd, lrs_o,
+                         extra=parity.BF16_REL * np.abs(lrs_o), what=("fused tail", k))
+    mu32 = np.float64(np.float32(wl.mu))
+    for i in pick:
+        r, c = wl.shapes[i]
+        g = G_m[i].astype(np.float64)
+        X = parity.bf16_round((mu32 * g + g).astype(np.float32)).astype(np.float64).reshape(r, c)
+        off = lay.full_offsets[i]
+        O = full[off: off + r * c].view(r, c).double().cpu().numpy()
+        rep = parity.check_ns(O, ref.newton_schulz(X, wl.ns_steps), 0, (i, (r, c), k))
+        print("NS fused", i, (r, c), k, rep)
+    del W, G, ws, full
+    torch.cuda.empty_cache()
