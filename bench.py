@@ -62,9 +62,8 @@ def elementwise_bytes(n_matrix_elems, ns_dtype):
 
 # DRAM bytes per Newton-Schulz launch (mean over the 15 launches of one step: Gram, Poly,
 # Update x 5, the last Update also applying W), measured with ncu on two Llama-3-8B layers
-# with the same kernel shape and scaled by 16 to the 32-layer set (profiles/
-# ns_tc_kernels_llama3_8b_x2.md).  Valid only for the kernel shape and the sources it was
-# taken with.
+# with the same kernel shape and scaled by 16 to the 32-layer set.  Valid only for the
+# kernel shape and the sources it was taken with.
 NS_TRAFFIC = {
     "llama3_8b_x32": {"bytes_per_launch": 16 * (23543323392 + 9060599296) / 15,
                       "tile_shape": 3,
@@ -108,7 +107,6 @@ def ns_traffic(workload, ns_dtype, kernel):
 NS_KERNEL_NAMES = {
     1: "ns_tc_single_kernel (tcgen05 cta_group::1, 128x256 tiles)",
     2: "ns_tc_pair_kernel (tcgen05 cta_group::2, 256x256 tiles)",
-    3: "ns_tc_mcast_kernel (2-CTA clusters, cta_group::1 per CTA, multicast B, 256x256 tiles)",
 }
 
 
@@ -134,9 +132,23 @@ def load_peaks():
             p = json.load(f)
         return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
                 "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "sm_mhz_under_load": (p.get("clocks_under_load") or {}).get("sm_mhz_median"),
                 "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
-            "source": "fallback"}
+            "sm_mhz_under_load": None, "source": "fallback"}
+
+
+def per_mhz(tflops, sm_mhz, peaks):
+    """TFLOP/s per MHz of SM clock, next to the cuBLAS sustained figure per MHz of the clock
+    it ran at, so that a clock advantage is not read as kernel efficiency."""
+    ref_mhz = peaks.get("sm_mhz_under_load")
+    out = {"ns_tflops_per_mhz": tflops / sm_mhz if sm_mhz else None,
+           "cublas_sustained_tflops_per_mhz":
+               peaks["bf16_tflops_sustained"] / ref_mhz if ref_mhz else None,
+           "ns_sm_mhz": sm_mhz, "cublas_sm_mhz": ref_mhz}
+    if out["ns_tflops_per_mhz"] and out["cublas_sustained_tflops_per_mhz"]:
+        out["ratio"] = out["ns_tflops_per_mhz"] / out["cublas_sustained_tflops_per_mhz"]
+    return out
 
 
 class ClockSampler:
@@ -221,56 +233,86 @@ def _shape_classes(wl):
     return classes
 
 
+def bench_config(wl, ns_dtype):
+    """The workload description both arms print (identical for the same arguments)."""
+    n = wl.numel
+    l2 = ("inputs larger than L2 (%.1f GB per fp32 buffer); no flush" % (4 * n / 1e9)
+          if 4 * n > 129e6 else
+          "inputs smaller than L2 (%.1f MB per fp32 buffer); no flush" % (4 * n / 1e6))
+    return {"workload": wl.name, "matrices": wl.n_matrices, "elements": n,
+            "n_shards": wl.n_shards, "ns_steps": wl.ns_steps, "ns_dtype": ns_dtype, "l2": l2}
+
+
+def _cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def _estimate(classes, times):
+    """Whole-step estimate: every shape class's mean one-matrix time x its matrix count."""
+    return sum(count * statistics.mean(times[key]) for key, count in classes)
+
+
+def _method(wl, ns_steps):
+    return (f"fp64 numpy oracle: one full step (momentum, {ns_steps} Newton-Schulz iterations, "
+            f"apply) of one matrix per distinct shape class (a matrix and its transpose share "
+            f"a class), each class's mean time x its matrix count, summed over the "
+            f"{len(_shape_classes(wl))} classes of the {wl.n_matrices}-matrix workload")
+
+
 def cpu_baseline(wl, ns_steps):
-    """The oracle on one matrix of each distinct shape, extrapolated to the whole step."""
-    total = 0.0
+    """The oracle on one matrix of each distinct shape, extrapolated to the whole step by
+    the shape counts (the same method as the reference arm)."""
+    classes = sorted(_shape_classes(wl).items(), key=lambda kv: kv[0][0] * kv[0][1])
+    times = {}
     spent = 0.0
-    done = []
-    for (n, m), count in sorted(_shape_classes(wl).items(), key=lambda kv: kv[0][0] * kv[0][1]):
+    for (n, m), _ in classes:
         t = _oracle_matrix_step_seconds(n, m, seed=n + m, ns_steps=ns_steps)
+        times[(n, m)] = [t]
         spent += t
-        total += count * t
-        done.append(f"{n}x{m}")
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return {"value": total * 1e3, "unit": "ms", "cores": cores, "kind": "oracle",
-            "sample": (f"fp64 numpy oracle, one full step (momentum, {ns_steps} NS iterations, "
-                       f"apply) of one matrix per distinct shape ({', '.join(done)}; a matrix "
-                       f"and its transpose share a shape), {spent:.1f} s of CPU work, "
-                       f"extrapolated to all {wl.n_matrices} matrices by shape counts"),
+    return {"value": _estimate(classes, times) * 1e3, "unit": "ms", "cores": _cores(),
+            "kind": "oracle",
+            "sample": _method(wl, ns_steps) + f"; one pass over the classes, {spent:.1f} s of CPU work",
             "sample_seconds": spent}
 
 
 def run_reference(args):
-    """The reference arm: the fp64 oracle, as it stands, on this host's cores."""
+    """The reference arm: the fp64 oracle, as it stands, on this host's cores.
+
+    Each timed step is a bounded sample: one matrix step of one shape class, the classes
+    taken in turn (all classes in every step when there are fewer steps than classes).
+    The line reports the whole-step estimate built from those samples, the same method as
+    the cpu_baseline leg of the GPU arm."""
     from muon_optimizer_step_gb300 import inputs
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     wl = inputs.WORKLOADS[args.workload]
     ns_steps = wl.ns_steps
-    _, dense_total = ns_flops(wl.shapes, wl.is_matrix, ns_steps)
-    # Per step: one bounded sample (the largest square-ish class that keeps a step to a few
-    # seconds), extrapolated by Newton-Schulz flops to the whole workload.
     classes = sorted(_shape_classes(wl).items(), key=lambda kv: kv[0][0] * kv[0][1])
-    n, m = classes[0][0]
-    for (nn, mm), _ in classes:
-        if nn * mm <= 4096 * 4096:
-            n, m = nn, mm
-    _, dense_sample = ns_flops([(n, m)], [True], ns_steps)
-    scale = dense_total / dense_sample
-    for _ in range(args.warmup):
-        _oracle_matrix_step_seconds(n, m, 7, ns_steps)
-    times = [_oracle_matrix_step_seconds(n, m, 7, ns_steps) * scale for _ in range(args.steps)]
-    ms = 1e3 * statistics.mean(times)
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    sample = (f"fp64 numpy oracle, one {n}x{m} matrix step per timed step, scaled by "
-              f"Newton-Schulz flops x{scale:.1f} to the {wl.n_matrices}-matrix workload")
+    small = classes[0][0]
+    for _ in range(args.warmup):  # warms the BLAS threads on the cheapest class
+        _oracle_matrix_step_seconds(small[0], small[1], 7, ns_steps)
+    times = {key: [] for key, _ in classes}
+    per_step = []
+    t_all = time.perf_counter()
+    for k in range(args.steps):
+        todo = [classes[k % len(classes)][0]] if args.steps >= len(classes) else \
+            [key for key, _ in classes]
+        t0 = time.perf_counter()
+        for (n, m) in todo:
+            times[(n, m)].append(_oracle_matrix_step_seconds(n, m, 7 + k, ns_steps))
+        per_step.append(time.perf_counter() - t0)
+    wall = time.perf_counter() - t_all
+    ms = _estimate(classes, times) * 1e3
+    cores = _cores()
+    sample = (_method(wl, ns_steps) + f"; {args.steps} timed steps, each one bounded sample "
+              f"(one class in turn), {wall:.1f} s of CPU work")
     line = {"impl": "reference", "metric": METRIC, "value": ms, "unit": "ms",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "matrices": wl.n_matrices, "elements": wl.numel,
-                       "ns_steps": ns_steps},
+            "config": bench_config(wl, args.ns_dtype),
+            "sample_seconds_per_step": per_step,
             "cpu_baseline": {"value": ms, "unit": "ms", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": ms, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -418,9 +460,12 @@ def run_ours(args):
 
     # ------------------------------------------------------------ end to end (host buffers)
     # Every step takes its gradient from pinned host memory and returns its updated
-    # weights to pinned host memory, through the public stage calls.  The copies of
+    # weights to pinned host memory, through the same public calls the timed step makes
+    # (stage 1, then the orthogonalization whose last Update applies W).  The copies of
     # neighbouring steps are pipelined on two copy streams: step t+1's gradient goes up
-    # while step t orthogonalizes, step t's weights go down while step t+1 starts.
+    # while step t runs; step t's weights are snapshot on the device (a device copy right
+    # after the step, so that step t+1 may update W while they travel) and go down while
+    # step t+1 runs.
     e2e = None
     if not args.no_e2e:
         need = 2 * 4 * N
@@ -433,6 +478,7 @@ def run_ours(args):
             G_h.copy_(Gb[:N])
             os.sched_setaffinity(0, saved_affinity)
             G2b = torch.empty_like(Gb)
+            W_snap = torch.empty(N, dtype=torch.float32, device=dev)
             gbufs = [Gb, G2b]
             h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
             comp = torch.cuda.current_stream()
@@ -440,7 +486,7 @@ def run_ours(args):
             ev = lambda: torch.cuda.Event()  # noqa: E731
             ev_in = [ev(), ev()]
             ev_k1 = [ev(), ev()]
-            ev_apply = [ev() for _ in range(n_e2e)]
+            ev_snap = [ev() for _ in range(n_e2e)]
             ev_out = [ev() for _ in range(n_e2e)]
             torch.cuda.synchronize()
             barrier()
@@ -463,14 +509,14 @@ def run_ours(args):
                             h2d.wait_event(ev_k1[(t + 1) % 2])
                         gbufs[(t + 1) % 2][:N].copy_(G_h, non_blocking=True)
                         ev_in[(t + 1) % 2].record(h2d)
-                capi.muon_orthogonalize_updates(lay, ws, ns_steps)
+                capi.muon_orthogonalize_apply(W, lay, ws, wl.lr, wl.wd, ns_steps)
                 if t >= 1:
-                    comp.wait_event(ev_out[t - 1])
-                capi.muon_apply_local_updates(W, lay, ws, wl.lr, wl.wd, ns_steps)
-                ev_apply[t].record(comp)
+                    comp.wait_event(ev_out[t - 1])  # the snapshot buffer is free again
+                W_snap.copy_(Wb[:N])
+                ev_snap[t].record(comp)
                 with torch.cuda.stream(d2h):
-                    d2h.wait_event(ev_apply[t])
-                    W_h.copy_(Wb[:N], non_blocking=True)
+                    d2h.wait_event(ev_snap[t])
+                    W_h.copy_(W_snap, non_blocking=True)
                     ev_out[t].record(d2h)
             comp.wait_event(ev_out[n_e2e - 1])
             b.record(comp)
@@ -479,10 +525,12 @@ def run_ours(args):
             e2e_ms = reduce_max_over_ranks([e2e_ms], dist, dev)[0]
             e2e = {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": 4 * N,
                    "d2h_bytes_per_step": 4 * N, "steps": n_e2e,
-                   "note": "per step: gradient H2D from pinned host memory, the three stage "
-                           "calls, updated weights D2H to pinned host memory; copies of "
-                           "neighbouring steps overlap compute on two copy streams"}
-            del G_h, W_h, G2b
+                   "note": "per step: gradient H2D from pinned host memory, "
+                           "muon_compute_momentum_inputs + muon_orthogonalize_apply (the "
+                           "calls muon_step makes), a device snapshot of W, W D2H to pinned "
+                           "host memory; copies of neighbouring steps overlap compute on two "
+                           "copy streams"}
+            del G_h, W_h, G2b, W_snap
         else:
             e2e = {"value": None, "unit": "ms", "h2d_bytes_per_step": 4 * N,
                    "d2h_bytes_per_step": 4 * N,
@@ -532,9 +580,7 @@ def run_ours(args):
                            "split": "tensor cores, fp32 operands split into three bf16 "
                                     "parts, six bf16 products each, fp32 accumulation"}[args.ns_dtype],
         "data": "synthetic",
-        "config": {"workload": wl.name, "matrices": wl.n_matrices, "elements": N,
-                   "n_shards": wl.n_shards, "ns_steps": ns_steps, "ns_dtype": args.ns_dtype,
-                   "l2": "inputs larger than L2 (%.1f GB per fp32 buffer); no flush" % (4 * N / 1e9)},
+        "config": bench_config(wl, args.ns_dtype),
         "ns_ms": ns_ms, "ns_tflops": ns_tflops, "ns_tflops_dense_equiv": dense / (ns_ms * 1e-3) / 1e12,
         "ns_flops_sym": sym, "matrices_per_s": wl.n_matrices / (ms * 1e-3),
         "stage_ms": {"momentum_inputs": stage_ms[0], "orthogonalize_apply": stage_ms[1]},
@@ -543,6 +589,11 @@ def run_ours(args):
                      "kernel": ns_kernel_label(ns_kernel, ns_steps, args.ns_dtype),
                      "achieved": ns_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": ns_tflops / peak_tc,
+                     "frac_of_burst": (ns_tflops / peaks["bf16_tflops"]
+                                       if args.ns_dtype == "bf16" else None),
+                     "peak_burst": peaks["bf16_tflops"] if args.ns_dtype == "bf16" else None,
+                     "per_mhz": (per_mhz(ns_tflops, (clocks or {}).get("sm_mhz"), peaks)
+                                 if args.ns_dtype == "bf16" else None),
                      "traffic": ns_traffic(wl.name, args.ns_dtype, ns_kernel),
                      "traffic_unit": "DRAM bytes per launch (ncu, mean over phases)",
                      "peak_note": peak_note},
