@@ -57,7 +57,9 @@ typedef enum muon_status {
   MUON_ERR_CUDA = 3,          /* a CUDA runtime call failed (message has the error)    */
   MUON_ERR_TIMEOUT = 4,       /* a device-side wait ran out of its budget              */
   MUON_ERR_OOM = 5,           /* host or device table allocation failed                */
-  MUON_ERR_UNSUPPORTED = 6    /* no sm_103a device, or a size beyond the library limits */
+  MUON_ERR_UNSUPPORTED = 6,   /* no sm_103a device, or a size beyond the library limits */
+  MUON_ERR_DEVICE_CHECK = 7   /* debug builds: a device-side range check of a table     */
+                              /* entry failed; the work it drove was skipped            */
 } muon_status;
 
 typedef enum muon_ns_dtype {
@@ -228,9 +230,10 @@ muon_status muon_export_update(const muon_layout* layout, const void* workspace,
  * MUON_ERR_UNSUPPORTED and a message giving both sizes.  The call allocates no device
  * memory (no cudaMalloc, cudaFree or allocating library routine); it uses host memory for
  * planning and cudaMemcpyAsync into the array.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  All calls share the array and leave their data in it:
- * calls that overlap on the GPU (different streams or threads) race.  Results equal those
+ * array's device address (cudaGetSymbolAddress) and zeroes the error word kept at its
+ * start, with that device current; make that first call before any stream capture.
+ * All calls share the array and leave their data in it: calls that overlap on the GPU
+ * (different streams or threads) race.  Results equal those
  * of muon_orthogonalize_full on an fp32 layout. */
 muon_status muon_orthogonalize_full_noalloc(const muon_layout* layout, const float* full_in,
                                             float* full_out, int32_t ns_steps,
@@ -238,7 +241,8 @@ muon_status muon_orthogonalize_full_noalloc(const muon_layout* layout, const flo
 
 /* ---------------------------------------------------------------- status
  * Synchronises `stream`, then reports a device-side wait timeout recorded since the last
- * check (MUON_ERR_TIMEOUT, and clears it) or a CUDA error (MUON_ERR_CUDA). */
+ * check (MUON_ERR_TIMEOUT, and clears it), a failed range check of a debug build
+ * (MUON_ERR_DEVICE_CHECK, and clears it) or a CUDA error (MUON_ERR_CUDA). */
 muon_status muon_check(cudaStream_t stream);
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* muon_last_error(void);
@@ -260,6 +264,25 @@ muon_status muon_layout_ns_kernel(const muon_layout* layout, int32_t* tile_shape
  * arrives on, with a budget of budget_cycles clock cycles (1..2^40).  The wait runs out,
  * the kernel records MUON_ERR_TIMEOUT and returns; a following muon_check reports it. */
 muon_status muon_selftest_wait_timeout(int64_t budget_cycles, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- debug builds
+ * A library built with -DMUON_DEBUG (muon_optimizer_step_gb300.csrc.build --debug, which
+ * writes libmuon_debug.so) checks every table entry inside the kernels before the access
+ * it drives: chunk records (matrix index, extent, shard index and offset of the first and
+ * last element, non-null shard pointers), matrix records (shape, pitches, workspace
+ * buffers inside the workspace, flat extent inside the shards) and tile records (matrix
+ * index, origin on the tile grid and inside the output, reduction length).  A failed
+ * check records MUON_ERR_DEVICE_CHECK in the device error word, the kernel skips that work
+ * (the tensor-core kernels skip their whole launch) and later kernels return at once
+ * until muon_check reports and clears it.  Nothing traps.  The pages have no counterpart.
+ * muon_debug_build: 1 in a debug build, 0 otherwise.
+ * muon_selftest_device_check: debug builds only (else MUON_ERR_UNSUPPORTED): runs the
+ * gather kernel on a one-chunk table whose chunk is longer than its matrix, built in a
+ * small buffer this call allocates (every access the chunk describes stays inside that
+ * buffer, so nothing can fault).  It synchronises `stream`; the following muon_check
+ * returns MUON_ERR_DEVICE_CHECK. */
+int32_t muon_debug_build(void);
+muon_status muon_selftest_device_check(cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -11,7 +11,9 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmuon.so")
+# MUON_LIB may name another build of the library (e.g. libmuon_debug.so, whose kernels
+# range-check every table entry they use); the default is the in-tree libmuon.so.
+LIB_PATH = os.environ.get("MUON_LIB") or os.path.join(_HERE, "libmuon.so")
 
 MUON_OK = 0
 MUON_ERR_INVALID_ARG = 1
@@ -20,6 +22,7 @@ MUON_ERR_CUDA = 3
 MUON_ERR_TIMEOUT = 4
 MUON_ERR_OOM = 5
 MUON_ERR_UNSUPPORTED = 6
+MUON_ERR_DEVICE_CHECK = 7
 MUON_NS_BF16 = 0
 MUON_NS_FP32 = 1
 MUON_NS_SPLIT_FP32 = 2
@@ -28,7 +31,7 @@ WORKSPACE_ALIGN = 1024
 
 _STATUS_NAMES = {0: "MUON_OK", 1: "MUON_ERR_INVALID_ARG", 2: "MUON_ERR_ALIGNMENT",
                  3: "MUON_ERR_CUDA", 4: "MUON_ERR_TIMEOUT", 5: "MUON_ERR_OOM",
-                 6: "MUON_ERR_UNSUPPORTED"}
+                 6: "MUON_ERR_UNSUPPORTED", 7: "MUON_ERR_DEVICE_CHECK"}
 
 # (name, restype, argtypes) of every entry point declared in include/muon.h.
 _P = ctypes.c_void_p
@@ -70,6 +73,8 @@ SIGNATURES = [
     ("muon_orthogonalize_full_noalloc", _I32, [_P, _P, _P, _I32, _P]),
     ("muon_check", _I32, [_P]),
     ("muon_selftest_wait_timeout", _I32, [_I64, _P]),
+    ("muon_debug_build", _I32, []),
+    ("muon_selftest_device_check", _I32, [_P]),
     ("muon_layout_ns_kernel", _I32, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32),
                                      ctypes.POINTER(_I32)]),
 ]
@@ -320,6 +325,15 @@ def muon_check_status(stream=None) -> int:
 def muon_selftest_wait_timeout(budget_cycles, stream=None):
     _check(lib.muon_selftest_wait_timeout(int(budget_cycles), _stream_handle(stream)),
            "muon_selftest_wait_timeout")
+
+
+def muon_debug_build() -> bool:
+    """Whether the loaded library was built with device-side range checks."""
+    return bool(lib.muon_debug_build())
+
+
+def muon_selftest_device_check(stream=None):
+    _check(lib.muon_selftest_device_check(_stream_handle(stream)), "muon_selftest_device_check")
 
 
 def muon_layout_ns_kernel(layout) -> dict:

@@ -129,6 +129,7 @@ muon_status ensure_device(muon_layout* L) {
     for (int p = 0; p < 3; ++p) {
       const TileList tl = plan_tiles(L->plan, p, kF32BM, kF32BN, 16, sms);
       t.grid[p] = tl.grid;
+      t.n_tiles[p] = (int64_t)tl.tiles.size();
       if ((s = upload(tl.tiles, &t.tiles[p])) != MUON_OK) { free_tables(&t); return s; }
       if ((s = upload(tl.cta_begin, &t.cta_begin[p])) != MUON_OK) { free_tables(&t); return s; }
     }
@@ -200,6 +201,7 @@ muon_status ensure_device(muon_layout* L) {
       while ((int)tl.cta_begin.size() < t.tc_units + 1) tl.cta_begin.push_back(tl.cta_begin.back());
       for (const TileDev& td : tl.tiles) L->plan.mats[td.mat].sig[p] += cluster ? 2 : 1;
       t.grid[p] = tl.grid;
+      t.n_tiles[p] = (int64_t)tl.tiles.size();
       if ((s = upload(tl.tiles, &t.tiles[p])) != MUON_OK) { free_tables(&t); return s; }
       if ((s = upload(tl.cta_begin, &t.cta_begin[p])) != MUON_OK) { free_tables(&t); return s; }
     }
@@ -649,10 +651,22 @@ muon_status muon_check(cudaStream_t stream) {
   int h = 0;
   e = cudaMemcpy(&h, word, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
+  // The allocation-free entry point keeps its own error word in its scratch array.
+  int h2 = 0;
+  int* word2 = noalloc_error_word(dev);
+  if (word2 != nullptr) {
+    e = cudaMemcpy(&h2, word2, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
+    if (h2 != 0) cudaMemset(word2, 0, sizeof(int));
+  }
+  if (h == 0) h = h2;
   if (h != 0) {
     cudaMemset(word, 0, sizeof(int));
     if (h == MUON_ERR_TIMEOUT)
       return fail(MUON_ERR_TIMEOUT, "a device-side wait ran out of its budget and the kernel exited");
+    if (h == MUON_ERR_DEVICE_CHECK)
+      return fail(MUON_ERR_DEVICE_CHECK, "a device-side range check of a table entry failed "
+                  "(debug build); the work it drove was skipped");
     return fail(MUON_ERR_CUDA, "device error word %d", h);
   }
   e = cudaGetLastError();
@@ -671,6 +685,58 @@ muon_status muon_layout_ns_kernel(const muon_layout* layout, int32_t* tile_shape
   *tile_shape = tc ? L->dt.tc_shape : 0;
   *units = tc ? L->dt.tc_units : 0;
   *persistent = tc && L->dt.tc_persistent ? 1 : 0;
+  return ok();
+}
+
+int32_t muon_debug_build(void) { return kDebugChecks ? 1 : 0; }
+
+muon_status muon_selftest_device_check(cudaStream_t stream) {
+  if (!kDebugChecks)
+    return fail(MUON_ERR_UNSUPPORTED, "this library was built without -DMUON_DEBUG");
+  int dev = -1;
+  MUON_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // One 2 x 4 matrix and one chunk of 16 elements: longer than the matrix, so the check
+  // must refuse it.  Shard and full buffers hold 64 floats, so even an unchecked copy of
+  // the chunk would stay inside them.
+  Plan plan;
+  plan.n_params = 1;
+  plan.n_shards = 1;
+  plan.ns_dtype = MUON_NS_FP32;
+  plan.N = 8;
+  plan.L = 16;
+  plan.full_numel = 8;
+  plan.ws_bytes = 1 << 20;
+  MatDev m{};
+  m.rows = 2; m.cols = 4; m.m = 2; m.n = 4; m.tall = 0; m.ldx = 8; m.lda = 8;
+  m.scale = 1.f; m.chunk_begin = 0; m.chunk_end = 1;
+  ChunkDev c{};
+  c.mat = 0; c.shard = 0; c.shard_off = 0; c.local = 0; c.len = 16; c.vec = 1;
+  plan.mats.push_back(m);
+  plan.chunks.push_back(c);
+  uint8_t* buf = nullptr;
+  const size_t bytes = 256 + 256 + 2 * 64 * sizeof(float);
+  MUON_CUDA(cudaMalloc(&buf, bytes), "cudaMalloc(selftest tables)");
+  cudaMemsetAsync(buf, 0, bytes, stream);
+  cudaMemcpyAsync(buf, &c, sizeof(c), cudaMemcpyHostToDevice, stream);
+  cudaMemcpyAsync(buf + 256, &m, sizeof(m), cudaMemcpyHostToDevice, stream);
+  DevTables dt;
+  dt.device = dev;
+  dt.n_sms = sms;
+  muon_status st = err_word(dev, &dt.err);
+  if (st != MUON_OK) { cudaFree(buf); return st; }
+  dt.chunks = reinterpret_cast<ChunkDev*>(buf);
+  dt.mats = reinterpret_cast<MatDev*>(buf + 256);
+  ShardPtrs sp;
+  std::memset(&sp, 0, sizeof(sp));
+  sp.p[0] = reinterpret_cast<float*>(buf + 512);
+  float* full = reinterpret_cast<float*>(buf + 512 + 64 * sizeof(float));
+  cudaError_t e = launch_gather(plan, dt, sp, full, stream);
+  const cudaError_t e2 = cudaStreamSynchronize(stream);
+  cudaFree(buf);
+  if (e != cudaSuccess) return cuda_fail(e, "selftest gather");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaStreamSynchronize");
   return ok();
 }
 

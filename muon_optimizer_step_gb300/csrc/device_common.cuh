@@ -10,12 +10,115 @@
 
 namespace muon {
 
-constexpr int kErrTimeout = 4;  // matches MUON_ERR_TIMEOUT
+constexpr int kErrTimeout = 4;      // matches MUON_ERR_TIMEOUT
+constexpr int kErrDeviceCheck = 7;  // matches MUON_ERR_DEVICE_CHECK
 
 // Kernel arguments: up to 128 shard base pointers, passed by value.
 struct ShardPtrs {
   float* p[128];
 };
+
+// ------------------------------------------------------------------ debug range checks
+// A debug build (compiled with -DMUON_DEBUG) checks, inside the kernels that use them,
+// every table entry before any access it drives: chunk records (matrix index, extent,
+// the shard index and offset of their first and last element, non-null shard pointers),
+// matrix records (shape, pitches, workspace buffers inside the workspace, flat extent
+// inside the shards) and tile records (matrix index, tile origin on the tile grid and
+// inside the phase's output, reduction length).  A failed check records
+// MUON_ERR_DEVICE_CHECK in the device error word and the kernel skips the work the entry
+// drives (or, for the pipelined tensor-core kernels, the whole launch); kernels that
+// start after a failed check return at once.  Nothing traps.  Release builds compile the
+// checks away.
+#ifdef MUON_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
+// What the checks compare against (passed to the kernels by value in every build).
+struct DebugCtx {
+  int* err;          // device error word
+  int32_t n_mats;
+  int32_t n_shards;
+  int64_t L;         // shard length (elements)
+  int64_t ws_bytes;  // workspace bytes
+  int32_t ns_dtype;  // 0 bf16, 1 fp32, 2 split fp32
+  int32_t pad_;
+};
+
+__device__ __forceinline__ bool debug_fail(const DebugCtx& d) {
+  atomicExch(d.err, kErrDeviceCheck);
+  return false;
+}
+
+// A failed check earlier in the stream (kept until muon_check clears it).
+__device__ __forceinline__ bool debug_halted(const DebugCtx& d) {
+  return kDebugChecks && *reinterpret_cast<volatile int*>(d.err) == kErrDeviceCheck;
+}
+
+__device__ __forceinline__ int64_t debug_buf_bytes(int64_t elems, int32_t ns_dtype) {
+  const int64_t esz = ns_dtype == 1 ? 4 : 2;
+  const int64_t parts = ns_dtype == 2 ? 3 : 1;
+  const int64_t one = (elems * esz + kWsAlign - 1) / kWsAlign * kWsAlign;
+  return one * parts;
+}
+
+__device__ __forceinline__ bool debug_mat_ok(const MatDev& mt, const DebugCtx& d) {
+  if (mt.rows < 1 || mt.cols < 1) return false;
+  if (mt.m != min(mt.rows, mt.cols) || mt.n != max(mt.rows, mt.cols)) return false;
+  if (mt.tall != (mt.rows > mt.cols ? 1 : 0)) return false;
+  if (mt.ldx < mt.cols || mt.lda < mt.m) return false;
+  const int64_t xb = debug_buf_bytes((int64_t)mt.rows * mt.ldx, d.ns_dtype);
+  const int64_t ab = debug_buf_bytes((int64_t)mt.m * mt.lda, d.ns_dtype);
+  if (mt.x0 < 0 || mt.x0 + xb > d.ws_bytes || mt.x1 < 0 || mt.x1 + xb > d.ws_bytes) return false;
+  if (mt.a < 0 || mt.a + ab > d.ws_bytes || mt.b < 0 || mt.b + ab > d.ws_bytes) return false;
+  if ((mt.x0 | mt.x1 | mt.a | mt.b) % kWsAlign != 0) return false;
+  const int64_t numel = (int64_t)mt.rows * mt.cols;
+  if (mt.flat_off < 0 || mt.flat_off + numel > d.L * d.n_shards) return false;
+  if (mt.group < 0 || mt.group >= kMaxGroups) return false;
+  return true;
+}
+
+// Non-null shard pointers for the flat range [g0, g1) (g1 > g0).
+__device__ __forceinline__ bool debug_shards_ok(const ShardPtrs& P, int64_t g0, int64_t g1,
+                                                const DebugCtx& d) {
+  const int64_t s0 = g0 / d.L, s1 = (g1 - 1) / d.L;
+  if (s0 < 0 || s1 >= d.n_shards || s1 >= 128) return false;
+  for (int64_t s = s0; s <= s1; ++s)
+    if (P.p[s] == nullptr) return false;
+  return true;
+}
+
+// Checks a chunk record and its matrix; P (may be null) are the shards it reads or
+// writes.  Records the failure; returns whether the chunk may be used.
+__device__ __forceinline__ bool debug_chunk_ok(const ChunkDev& ch, const MatDev* mats,
+                                               const DebugCtx& d, const ShardPtrs* P) {
+  if (ch.mat < 0 || ch.mat >= d.n_mats) return debug_fail(d);
+  const MatDev& mt = mats[ch.mat];
+  if (!debug_mat_ok(mt, d)) return debug_fail(d);
+  const int64_t numel = (int64_t)mt.rows * mt.cols;
+  if (ch.len < 1 || ch.local < 0 || ch.local + ch.len > numel) return debug_fail(d);
+  const int64_t g0 = mt.flat_off + ch.local;
+  if (ch.shard != g0 / d.L || ch.shard_off != g0 - (int64_t)ch.shard * d.L) return debug_fail(d);
+  if (ch.vec && ch.shard_off + ch.len > d.L) return debug_fail(d);
+  if (P != nullptr && !debug_shards_ok(*P, g0, g0 + ch.len, d)) return debug_fail(d);
+  return true;
+}
+
+// Checks a tile record of `phase` on a bm x bn tile grid with k-blocks of bk.
+__device__ __forceinline__ bool debug_tile_ok(const TileDev& t, int phase, const MatDev* mats,
+                                              const DebugCtx& d, int bm, int bn, int bk) {
+  if (t.mat < 0 || t.mat >= d.n_mats) return false;
+  const MatDev& mt = mats[t.mat];
+  if (!debug_mat_ok(mt, d)) return false;
+  const int mo = phase == kPhaseUpdate ? mt.rows : mt.m;
+  const int no = phase == kPhaseUpdate ? mt.cols : mt.m;
+  const int K = phase == kPhaseGram ? mt.n : mt.m;
+  if (t.i0 < 0 || t.i0 >= mo || t.i0 % bm != 0) return false;
+  if (t.j0 < 0 || t.j0 >= no || t.j0 % bn != 0) return false;
+  if (t.kblocks != (K + bk - 1) / bk) return false;
+  return true;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -311,6 +414,12 @@ struct ApplyArgs {
   long long L;     // shard length
   GroupParams gp;  // lr and decay per group
 };
+
+// Debug builds: the shards a matrix's apply writes exist.
+__device__ __forceinline__ bool debug_apply_ok(const ApplyArgs& ap, const MatDev& mt,
+                                               const DebugCtx& d) {
+  return debug_shards_ok(ap.W, mt.flat_off, mt.flat_off + (int64_t)mt.rows * mt.cols, d);
+}
 
 // W <- W * decay - lr * scale * O for the elements (i, jb .. jb + n - 1) of a matrix, whose
 // row-major element (i, j) lives at flat index flat_off + i * cols + j of the sharded

@@ -79,12 +79,25 @@ __device__ __forceinline__ void store_slice(const OpDesc& op, const float (&r)[8
 __global__ void __launch_bounds__(NT)
 ns_phase_f32_kernel(const TileDev* __restrict__ tiles, const int32_t* __restrict__ cta_begin,
                     const MatDev* __restrict__ mats, uint8_t* __restrict__ ws,
-                    const float* __restrict__ inv_norm, int phase, int x_in, int iter0) {
+                    const float* __restrict__ inv_norm, int phase, int x_in, int iter0,
+                    int64_t n_tiles, const DebugCtx dbg) {
   __shared__ __align__(16) float As[BK][BM + PAD];
   __shared__ __align__(16) float Bs[BK][BN + PAD];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  if (debug_halted(dbg)) return;
+  if (kDebugChecks) {
+    const int b0 = cta_begin[blockIdx.x], b1 = cta_begin[blockIdx.x + 1];
+    if (b0 < 0 || b1 < b0 || b1 > n_tiles) {
+      if (threadIdx.x == 0) debug_fail(dbg);
+      return;
+    }
+  }
   for (int ti = cta_begin[blockIdx.x]; ti < cta_begin[blockIdx.x + 1]; ++ti) {
     const TileDev tile = tiles[ti];
+    if (kDebugChecks && !debug_tile_ok(tile, phase, mats, dbg, BM, BN, BK)) {
+      if (threadIdx.x == 0) debug_fail(dbg);
+      continue;
+    }
     const MatDev mt = mats[tile.mat];
     const float* xin = reinterpret_cast<const float*>(ws + (x_in ? mt.x1 : mt.x0));
     float* xout = reinterpret_cast<float*>(ws + (x_in ? mt.x0 : mt.x1));
@@ -180,7 +193,8 @@ cudaError_t launch_ns_phase_f32(const Plan& plan, const DevTables& dt, void* ws,
   uint8_t* w = static_cast<uint8_t*>(ws);
   ns_phase_f32_kernel<<<grid, NT, 0, st>>>(dt.tiles[phase], dt.cta_begin[phase], dt.mats, w,
                                            reinterpret_cast<const float*>(w + plan.ws_inv_norm),
-                                           phase, x_in, iter0);
+                                           phase, x_in, iter0, dt.n_tiles[phase],
+                                           make_debug_ctx(plan, dt));
   return cudaGetLastError();
 }
 

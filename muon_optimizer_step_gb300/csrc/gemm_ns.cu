@@ -101,7 +101,31 @@ struct NsParams {
   int q_begin, q_end;        // this launch runs phases q = 3*it + phase in [q_begin, q_end)
   int apply;                 // last Update also applies the step to W
   ApplyArgs ap;
+  int64_t n_tiles[3];        // entries of each phase's tile list
+  DebugCtx dbg;
 };
+
+// Debug builds: every tile this CTA (pair) will run in this launch, checked before any
+// role starts.  The answer depends on the tables only, so both CTAs of a pair reach the
+// same one and leave together.
+template <int kShape>
+__device__ __forceinline__ bool debug_tiles_ok(const NsParams& p, int unit) {
+  constexpr int bm = kShape == kShapeSingle ? 128 : 256;
+  for (int phase = 0; phase < 3; ++phase) {
+    bool used = false;
+    for (int qq = p.q_begin; qq < p.q_end; ++qq) used |= (qq % 3) == phase;
+    if (!used) continue;
+    const int b0 = p.begin[phase][unit], b1 = p.begin[phase][unit + 1];
+    if (b0 < 0 || b1 < b0 || b1 > p.n_tiles[phase]) return false;
+    for (int ti = b0; ti < b1; ++ti) {
+      const TileDev t = p.tiles[phase][ti];
+      if (!debug_tile_ok(t, phase, p.mats, p.dbg, bm, BN, 64)) return false;
+      if (p.apply && phase == kPhaseUpdate && !debug_apply_ok(p.ap, p.mats[t.mat], p.dbg))
+        return false;
+    }
+  }
+  return true;
+}
 
 // Which tensor maps and transpose bits a tile of `phase` uses.
 struct TileOps {
@@ -511,6 +535,15 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = kCluster ? cluster_ctarank() : 0u;  // pair: 0 issues the MMAs
   const int unit = kCluster ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  if constexpr (kDebugChecks) {
+    __shared__ int dbg_bad;
+    if (threadIdx.x == 0) {
+      dbg_bad = debug_tiles_ok<kShape>(p, unit) ? 0 : 1;
+      if (dbg_bad) debug_fail(p.dbg);
+    }
+    __syncthreads();
+    if (dbg_bad) return;
+  }
   const uint32_t peer_abort = kCluster ? mapa_shared(smem_u32(&abort_flag), rank ^ 1u) : 0u;
   // This CTA issues MMAs (all but the odd CTA of a cta_group::2 pair).
   const bool mma_cta = !kTwoSm || rank == 0;
@@ -908,6 +941,8 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
   p.q_end = q_end;
   p.apply = ap != nullptr ? 1 : 0;
   if (ap != nullptr) p.ap = *ap;
+  for (int ph = 0; ph < 3; ++ph) p.n_tiles[ph] = dt.n_tiles[ph];
+  p.dbg = make_debug_ctx(plan, dt);
   cudaError_t e = cudaSuccess;
   if (q_end - q_begin > 1) {
     e = cudaMemsetAsync(p.counters, 0, plan.mats.size() * 3 * sizeof(int), st);

@@ -13,6 +13,7 @@ namespace muon {
 struct ShardPtrs;
 struct ApplyArgs;
 struct GroupParams;
+struct DebugCtx;
 
 // Tile shapes of the tcgen05 Newton-Schulz kernels (the values MUON_TC_KERNEL pins and
 // muon_layout_ns_kernel reports).
@@ -28,6 +29,7 @@ struct DevTables {
   int* err = nullptr;           // device error word (MUON_ERR_TIMEOUT when a wait gave up)
   TileDev* tiles[3] = {nullptr, nullptr, nullptr};
   int32_t* cta_begin[3] = {nullptr, nullptr, nullptr};
+  int64_t n_tiles[3] = {0, 0, 0};  // entries of each phase's tile list
   int grid[3] = {0, 0, 0};
   CUtensorMap* tmaps = nullptr; // kMapsPerMat per matrix (bf16 path)
   int tc_shape = kShapeSingle;  // bf16 path: tile shape (kShape*)
@@ -36,6 +38,9 @@ struct DevTables {
                                 // phase's cta_begin has tc_units + 1 entries
   const void* tmap_ws = nullptr;  // workspace the tensor maps were encoded for
 };
+
+// What the debug range checks of the kernels compare against (see DebugCtx).
+DebugCtx make_debug_ctx(const Plan& plan, const DevTables& dt);
 
 // Stage 1: momentum, orthogonalization input into X0, per-chunk sums of squares.
 cudaError_t launch_momentum_input(const Plan& plan, const DevTables& dt, const ShardPtrs& g,
@@ -77,5 +82,8 @@ bool encode_tensor_maps(const Plan& plan, const void* ws, std::vector<CUtensorMa
 cudaError_t launch_selftest_timeout(int* err, long long budget, cudaStream_t st);
 // Sets the message muon_last_error() returns on this thread.
 void set_last_error(const std::string& msg);
+// The allocation-free entry point's error word on device `dev` (inside its scratch
+// array), or nullptr if that entry point has not run there.
+int* noalloc_error_word(int dev);
 
 }  // namespace muon

@@ -27,9 +27,14 @@ using namespace muon;
 
 // The scratch array of this entry point: 32 MiB on every GPU where the library's device
 // code is loaded, held until the process exits.  Calls share it and leave their data in
-// it; calls that overlap on the GPU (two streams, two threads) race on it.
+// it; calls that overlap on the GPU (two streams, two threads) race on it.  It is
+// 1024-byte aligned, so offsets that are multiples of 1024 from its start are 1024-byte
+// aligned addresses, as the workspace must be.  Its first 256 bytes hold the error word
+// the kernels of a debug build write (zeroed when a device is set up; muon_check reads
+// and clears it).
 constexpr size_t kScratchBytes = (size_t)32 << 20;
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+constexpr size_t kErrSlot = 256;
+static __device__ __align__(1024) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDev = 64;
 void* g_scratch_addr[kMaxDev] = {nullptr};
@@ -38,12 +43,15 @@ std::mutex g_scratch_mu;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Device address of the scratch array on the current device; looked up once per device
-// (with that device current).  The host-side name g_noalloc_scratch is only a stand-in.
+// (with that device current), when its error word is also zeroed.  The host-side name
+// g_noalloc_scratch is only a stand-in.
 cudaError_t scratch_address(int dev, unsigned char** out) {
   std::lock_guard<std::mutex> g(g_scratch_mu);
   if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    e = cudaMemset(p, 0, kErrSlot);
     if (e != cudaSuccess) return e;
     g_scratch_addr[dev] = p;
   }
@@ -59,6 +67,12 @@ size_t place(size_t* off, size_t n, size_t align) {
 }
 
 }  // namespace
+
+int* muon::noalloc_error_word(int dev) {
+  if (dev < 0 || dev >= kMaxDev) return nullptr;
+  std::lock_guard<std::mutex> g(g_scratch_mu);
+  return static_cast<int*>(g_scratch_addr[dev]);
+}
 
 extern "C" muon_status muon_orthogonalize_full_noalloc(const muon_layout* layout,
                                                        const float* full_in, float* full_out,
@@ -97,9 +111,9 @@ extern "C" muon_status muon_orthogonalize_full_noalloc(const muon_layout* layout
   TileList tl[3];
   for (int p = 0; p < 3; ++p) tl[p] = plan_tiles(plan, p, kF32BM, kF32BN, 16, sms);
 
-  // Scratch map: tables first, then the workspace (1024-byte aligned, as the kernels
-  // expect).  Everything must fit in kScratchBytes.
-  size_t off = 0;
+  // Scratch map: the error word, the tables, then the workspace (1024-byte aligned, as
+  // the kernels expect).  Everything must fit in kScratchBytes.
+  size_t off = kErrSlot;
   const size_t o_chunks = place<ChunkDev>(&off, plan.chunks.size(), 256);
   const size_t o_mats = place<MatDev>(&off, plan.mats.size(), 256);
   size_t o_tiles[3], o_begin[3];
@@ -134,6 +148,7 @@ extern "C" muon_status muon_orthogonalize_full_noalloc(const muon_layout* layout
   DevTables dt;
   dt.device = dev;
   dt.n_sms = sms;
+  dt.err = reinterpret_cast<int*>(base);
   dt.chunks = reinterpret_cast<ChunkDev*>(base + o_chunks);
   dt.mats = reinterpret_cast<MatDev*>(base + o_mats);
   for (int p = 0; p < 3; ++p) {
@@ -144,10 +159,13 @@ extern "C" muon_status muon_orthogonalize_full_noalloc(const muon_layout* layout
     dt.tiles[p] = reinterpret_cast<TileDev*>(base + o_tiles[p]);
     dt.cta_begin[p] = reinterpret_cast<int32_t*>(base + o_begin[p]);
     dt.grid[p] = tl[p].grid;
+    dt.n_tiles[p] = (int64_t)tl[p].tiles.size();
   }
   // Nothing in the workspace has to start at zero: every slot a kernel reads (chunk sums,
   // 1/||X||, X0, X1, A, B) is written earlier in the same call.
   void* ws = base + o_ws;
+  if (reinterpret_cast<uintptr_t>(ws) % kWsAlign != 0)
+    return fail(MUON_ERR_ALIGNMENT, "scratch workspace is not 1024-byte aligned");
   if ((e = launch_full_input(plan, dt, full_in, ws, stream)) != cudaSuccess ||
       (e = launch_norm_finalize(plan, dt, ws, stream)) != cudaSuccess)
     return fail(MUON_ERR_CUDA, cudaGetErrorString(e));

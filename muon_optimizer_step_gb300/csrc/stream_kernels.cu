@@ -151,10 +151,13 @@ __global__ void __launch_bounds__(kThreads)
 momentum_input_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
                       const MatDev* __restrict__ mats, ShardPtrs G, ShardPtrs M, int64_t L,
                       uint8_t* __restrict__ ws, float* __restrict__ partials,
-                      const __grid_constant__ GroupParams gp) {
+                      const __grid_constant__ GroupParams gp, const DebugCtx dbg) {
   __shared__ float red[32];
+  if (debug_halted(dbg)) return;
   for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
     const ChunkDev ch = chunks[ci];
+    if (kDebugChecks && (!debug_chunk_ok(ch, mats, dbg, &G) || !debug_chunk_ok(ch, mats, dbg, &M)))
+      continue;
     const MatDev& mt = mats[ch.mat];
     const float mu = gp.mu[mt.group];
     const int nesterov = gp.nesterov[mt.group];
@@ -258,10 +261,12 @@ template <typename XT>
 __global__ void __launch_bounds__(kThreads)
 full_input_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
                   const MatDev* __restrict__ mats, const float* __restrict__ full,
-                  uint8_t* __restrict__ ws, float* __restrict__ partials) {
+                  uint8_t* __restrict__ ws, float* __restrict__ partials, const DebugCtx dbg) {
   __shared__ float red[32];
+  if (debug_halted(dbg)) return;
   for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
     const ChunkDev ch = chunks[ci];
+    if (kDebugChecks && !debug_chunk_ok(ch, mats, dbg, nullptr)) continue;
     const MatDev& mt = mats[ch.mat];
     const float* src = full + mt.full_off + ch.local;
     const typename XBuf<XT>::ptr x = XBuf<XT>::at(ws, mt.x0, mt);
@@ -278,10 +283,17 @@ full_input_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
 
 __global__ void __launch_bounds__(kThreads)
 norm_finalize_kernel(const MatDev* __restrict__ mats, int n_mats,
-                     const float* __restrict__ partials, float* __restrict__ inv_norm) {
+                     const float* __restrict__ partials, float* __restrict__ inv_norm,
+                     int64_t n_chunks, const DebugCtx dbg) {
   __shared__ double red[kThreads];
+  if (debug_halted(dbg)) return;
   for (int mi = blockIdx.x; mi < n_mats; mi += gridDim.x) {
     const MatDev& mt = mats[mi];
+    if (kDebugChecks && (mt.chunk_begin < 0 || mt.chunk_end > n_chunks ||
+                         mt.chunk_begin > mt.chunk_end)) {
+      if (threadIdx.x == 0) debug_fail(dbg);
+      continue;
+    }
     double s = 0.0;
     for (int64_t c = mt.chunk_begin + threadIdx.x; c < mt.chunk_end; c += kThreads)
       s += (double)partials[c];
@@ -302,9 +314,11 @@ apply_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
              const MatDev* __restrict__ mats, ShardPtrs W, int64_t L,
              const uint8_t* __restrict__ ws,
              int final_buf, const float* __restrict__ inv_norm, int pending_norm,
-             const __grid_constant__ GroupParams gp) {
+             const __grid_constant__ GroupParams gp, const DebugCtx dbg) {
+  if (debug_halted(dbg)) return;
   for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
     const ChunkDev ch = chunks[ci];
+    if (kDebugChecks && !debug_chunk_ok(ch, mats, dbg, &W)) continue;
     const MatDev& mt = mats[ch.mat];
     float lrs = gp.lr[mt.group] * mt.scale;
     const float decay = gp.decay[mt.group];
@@ -356,9 +370,12 @@ apply_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
 
 __global__ void __launch_bounds__(kThreads)
 gather_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
-              const MatDev* __restrict__ mats, ShardPtrs S, int64_t L, float* __restrict__ full) {
+              const MatDev* __restrict__ mats, ShardPtrs S, int64_t L, float* __restrict__ full,
+              const DebugCtx dbg) {
+  if (debug_halted(dbg)) return;
   for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
     const ChunkDev ch = chunks[ci];
+    if (kDebugChecks && !debug_chunk_ok(ch, mats, dbg, &S)) continue;
     float* dst = full + mats[ch.mat].full_off + ch.local;
     if (ch.vec) {
       const float* src = S.p[ch.shard] + ch.shard_off;
@@ -375,9 +392,11 @@ gather_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
 __global__ void __launch_bounds__(kThreads)
 scatter_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
                const MatDev* __restrict__ mats, const float* __restrict__ full, ShardPtrs D,
-               int64_t L) {
+               int64_t L, const DebugCtx dbg) {
+  if (debug_halted(dbg)) return;
   for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
     const ChunkDev ch = chunks[ci];
+    if (kDebugChecks && !debug_chunk_ok(ch, mats, dbg, &D)) continue;
     const float* src = full + mats[ch.mat].full_off + ch.local;
     if (ch.vec) {
       float* dst = D.p[ch.shard] + ch.shard_off;
@@ -395,9 +414,12 @@ template <typename XT>
 __global__ void __launch_bounds__(kThreads)
 export_kernel(const ChunkDev* __restrict__ chunks, int64_t n_chunks,
               const MatDev* __restrict__ mats, const uint8_t* __restrict__ ws, int buf,
-              const float* __restrict__ inv_norm, int pending_norm, float* __restrict__ full) {
+              const float* __restrict__ inv_norm, int pending_norm, float* __restrict__ full,
+              const DebugCtx dbg) {
+  if (debug_halted(dbg)) return;
   for (int64_t ci = blockIdx.x; ci < n_chunks; ci += gridDim.x) {
     const ChunkDev ch = chunks[ci];
+    if (kDebugChecks && !debug_chunk_ok(ch, mats, dbg, nullptr)) continue;
     const MatDev& mt = mats[ch.mat];
     const float s = pending_norm ? inv_norm[ch.mat] : 1.f;
     const typename XBuf<XT>::ptr x = XBuf<XT>::at(ws, buf ? mt.x1 : mt.x0, mt);
@@ -415,22 +437,34 @@ int grid_for(const Plan& plan, const DevTables& dt) {
 
 }  // namespace
 
+DebugCtx make_debug_ctx(const Plan& plan, const DevTables& dt) {
+  DebugCtx d{};
+  d.err = dt.err;
+  d.n_mats = (int32_t)plan.mats.size();
+  d.n_shards = plan.n_shards;
+  d.L = plan.L > 0 ? plan.L : 1;
+  d.ws_bytes = plan.ws_bytes;
+  d.ns_dtype = plan.ns_dtype;
+  return d;
+}
+
 cudaError_t launch_momentum_input(const Plan& plan, const DevTables& dt, const ShardPtrs& g,
                                   const ShardPtrs& m, void* ws, const GroupParams& gp,
                                   cudaStream_t st) {
   const int grid = grid_for(plan, dt);
   if (grid == 0) return cudaSuccess;
+  const DebugCtx dbg = make_debug_ctx(plan, dt);
   uint8_t* w = static_cast<uint8_t*>(ws);
   float* partials = reinterpret_cast<float*>(w + plan.ws_partials);
   if (plan.ns_dtype == 0)
     momentum_input_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
-        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, plan.L, w, partials, gp);
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, plan.L, w, partials, gp, dbg);
   else if (plan.ns_dtype == 1)
     momentum_input_kernel<float><<<grid, kThreads, 0, st>>>(
-        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, plan.L, w, partials, gp);
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, plan.L, w, partials, gp, dbg);
   else
     momentum_input_kernel<Bf16x3><<<grid, kThreads, 0, st>>>(
-        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, plan.L, w, partials, gp);
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, g, m, plan.L, w, partials, gp, dbg);
   return cudaGetLastError();
 }
 
@@ -438,17 +472,18 @@ cudaError_t launch_full_input(const Plan& plan, const DevTables& dt, const float
                               cudaStream_t st) {
   const int grid = grid_for(plan, dt);
   if (grid == 0) return cudaSuccess;
+  const DebugCtx dbg = make_debug_ctx(plan, dt);
   uint8_t* w = static_cast<uint8_t*>(ws);
   float* partials = reinterpret_cast<float*>(w + plan.ws_partials);
   if (plan.ns_dtype == 0)
     full_input_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
-        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, full, w, partials);
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, full, w, partials, dbg);
   else if (plan.ns_dtype == 1)
     full_input_kernel<float><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
-                                                        dt.mats, full, w, partials);
+                                                        dt.mats, full, w, partials, dbg);
   else
     full_input_kernel<Bf16x3><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
-                                                         dt.mats, full, w, partials);
+                                                         dt.mats, full, w, partials, dbg);
   return cudaGetLastError();
 }
 
@@ -460,7 +495,8 @@ cudaError_t launch_norm_finalize(const Plan& plan, const DevTables& dt, void* ws
   const int grid = n < 65535 ? n : 65535;
   norm_finalize_kernel<<<grid, kThreads, 0, st>>>(
       dt.mats, n, reinterpret_cast<const float*>(w + plan.ws_partials),
-      reinterpret_cast<float*>(w + plan.ws_inv_norm));
+      reinterpret_cast<float*>(w + plan.ws_inv_norm), (int64_t)plan.chunks.size(),
+      make_debug_ctx(plan, dt));
   return cudaGetLastError();
 }
 
@@ -469,20 +505,21 @@ cudaError_t launch_apply(const Plan& plan, const DevTables& dt, const ShardPtrs&
                          cudaStream_t st) {
   const int grid = grid_for(plan, dt);
   if (grid == 0) return cudaSuccess;
+  const DebugCtx dbg = make_debug_ctx(plan, dt);
   const uint8_t* w = static_cast<const uint8_t*>(ws);
   const float* inv = reinterpret_cast<const float*>(w + plan.ws_inv_norm);
   if (plan.ns_dtype == 0)
     apply_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
         dt.chunks, (int64_t)plan.chunks.size(), dt.mats, wp, plan.L, w, final_buf, inv,
-        pending_norm, gp);
+        pending_norm, gp, dbg);
   else if (plan.ns_dtype == 1)
     apply_kernel<float><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
                                                    dt.mats, wp, plan.L, w, final_buf, inv,
-                                                   pending_norm, gp);
+                                                   pending_norm, gp, dbg);
   else
     apply_kernel<Bf16x3><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
                                                     dt.mats, wp, plan.L, w, final_buf, inv,
-                                                    pending_norm, gp);
+                                                    pending_norm, gp, dbg);
   return cudaGetLastError();
 }
 
@@ -491,7 +528,7 @@ cudaError_t launch_gather(const Plan& plan, const DevTables& dt, const ShardPtrs
   const int grid = grid_for(plan, dt);
   if (grid == 0) return cudaSuccess;
   gather_kernel<<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(), dt.mats,
-                                           src, plan.L, full);
+                                           src, plan.L, full, make_debug_ctx(plan, dt));
   return cudaGetLastError();
 }
 
@@ -500,7 +537,7 @@ cudaError_t launch_scatter(const Plan& plan, const DevTables& dt, const float* f
   const int grid = grid_for(plan, dt);
   if (grid == 0) return cudaSuccess;
   scatter_kernel<<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(), dt.mats,
-                                            full, dst, plan.L);
+                                            full, dst, plan.L, make_debug_ctx(plan, dt));
   return cudaGetLastError();
 }
 
@@ -508,17 +545,18 @@ cudaError_t launch_export(const Plan& plan, const DevTables& dt, const void* ws,
                           int pending_norm, float* full, cudaStream_t st) {
   const int grid = grid_for(plan, dt);
   if (grid == 0) return cudaSuccess;
+  const DebugCtx dbg = make_debug_ctx(plan, dt);
   const uint8_t* w = static_cast<const uint8_t*>(ws);
   const float* inv = reinterpret_cast<const float*>(w + plan.ws_inv_norm);
   if (plan.ns_dtype == 0)
     export_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
-        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, w, buf, inv, pending_norm, full);
+        dt.chunks, (int64_t)plan.chunks.size(), dt.mats, w, buf, inv, pending_norm, full, dbg);
   else if (plan.ns_dtype == 1)
     export_kernel<float><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
-                                                    dt.mats, w, buf, inv, pending_norm, full);
+                                                    dt.mats, w, buf, inv, pending_norm, full, dbg);
   else
     export_kernel<Bf16x3><<<grid, kThreads, 0, st>>>(dt.chunks, (int64_t)plan.chunks.size(),
-                                                     dt.mats, w, buf, inv, pending_norm, full);
+                                                     dt.mats, w, buf, inv, pending_norm, full, dbg);
   return cudaGetLastError();
 }
 

@@ -144,3 +144,23 @@ def test_header_constants_match_the_binding():
             assert capi.muon_abi_version() == val
         else:
             assert getattr(capi, name) == val, name
+
+
+def test_debug_build_links_and_exports_the_same_symbols(tmp_path):
+    """The debug build (-DMUON_DEBUG) compiles, exports every declared symbol and says it
+    is a debug build; the release library says it is not.  No kernel runs."""
+    import subprocess
+    import sys
+    from muon_optimizer_step_gb300.csrc import build
+    lib = build.build(debug=True)
+    names = declared_symbols()
+    code = ("import ctypes, sys\n"
+            f"lib = ctypes.CDLL({lib!r})\n"
+            f"missing = [n for n in {names!r} if not hasattr(lib, n)]\n"
+            "assert not missing, missing\n"
+            "lib.muon_debug_build.restype = ctypes.c_int32\n"
+            "assert lib.muon_debug_build() == 1\n"
+            "print('ok')\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
+    assert not capi.muon_debug_build()
