@@ -188,6 +188,45 @@ muon_status muon_orthogonalize_apply(float* const* flat_params, const muon_layou
 muon_status muon_assign_owners(const muon_layout* layout, int32_t ns_steps, int32_t* owner,
                                double* rank_cost);
 
+/* ---------------------------------------------------------------- owner exchange plan
+ * [P1] "Opt step" step 3 gathers each sharded matrix's orthogonalization input on its
+ * owner and step 5 sends the owner's update back to the ranks that hold its shards ([P2]
+ * _FsdpGroupAssignment.tensor_to_owner_rank names that owner).  muon_exchange_plan lists
+ * the data plane of that exchange for a group of n_shards ranks (rank r holds shard r):
+ * every matrix parameter's flat range cut at shard edges into runs, each run moved from
+ * its shard on src_rank to the parameter's place in the owner's packed buffer on
+ * dst_rank (step 3), and back along the same run (step 5).  The packed buffer of a rank
+ * holds the parameters it owns, row-major, back to back in parameter order, each starting
+ * at a multiple of 4 elements; its parameters read there are the full matrices
+ * muon_gather_full builds, and runs written back reproduce muon_scatter_updates.
+ * Runs whose src_rank equals dst_rank are local copies.  Pure host work, deterministic.
+ *   owner          host array of n_params owners (muon_assign_owners' output works);
+ *                  entries of matrix parameters must lie in 0..n_shards-1, the others are
+ *                  ignored.
+ *   rank           the rank whose lists are wanted, 0..n_shards-1.
+ *   sends          runs with src_rank == rank, ordered by (dst_rank, parameter, offset);
+ *   recvs          runs with dst_rank == rank, ordered by (src_rank, parameter, offset).
+ *                  For each pair of ranks the sender's and the receiver's lists hold the
+ *                  same runs in the same order, so one message per peer can carry them
+ *                  back to back.  Either array may be NULL (then only its count is
+ *                  returned); otherwise *n_sends / *n_recvs give its capacity on entry
+ *                  (MUON_ERR_INVALID_ARG if too small) and the count on return.
+ *   owned_numel    receives the length of `rank`'s packed buffer (may be NULL).
+ *   owned_offsets  NULL or n_params entries: each parameter's offset in its owner's packed
+ *                  buffer (-1 for non-matrix parameters). */
+typedef struct muon_xfer {
+  int32_t param;      /* parameter index */
+  int32_t src_rank;   /* rank (= shard index) whose shard holds the run */
+  int32_t dst_rank;   /* the parameter's owner */
+  int32_t pad_;
+  int64_t shard_off;  /* element offset of the run in src_rank's shard */
+  int64_t owner_off;  /* element offset of the run in dst_rank's packed buffer */
+  int64_t len;        /* elements in the run */
+} muon_xfer;
+muon_status muon_exchange_plan(const muon_layout* layout, const int32_t* owner, int32_t rank,
+                               muon_xfer* sends, int64_t* n_sends, muon_xfer* recvs,
+                               int64_t* n_recvs, int64_t* owned_numel, int64_t* owned_offsets);
+
 /* ---------------------------------------------------------------- owner gather / scatter
  * [P1] "Opt step" step 3 (gather on the owner) and step 5 (scatter from the owner) as
  * pure index maps between the shards and the fp32 full layout.  Bit copies.

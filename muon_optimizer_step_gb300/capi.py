@@ -65,6 +65,9 @@ SIGNATURES = [
     ("muon_layout_set_groups", _I32, [_P, ctypes.POINTER(_I32), _I32]),
     ("muon_step_grouped", _I32, [_PP, _PP, _PP, _P, _P, ctypes.POINTER(GroupHparams), _I32, _P]),
     ("muon_assign_owners", _I32, [_P, _I32, ctypes.POINTER(_I32), ctypes.POINTER(ctypes.c_double)]),
+    ("muon_exchange_plan", _I32, [_P, ctypes.POINTER(_I32), _I32, _P, ctypes.POINTER(_I64), _P,
+                                  ctypes.POINTER(_I64), ctypes.POINTER(_I64),
+                                  ctypes.POINTER(_I64)]),
     ("muon_gather_full", _I32, [_P, _PP, _P, _P]),
     ("muon_scatter_updates", _I32, [_P, _P, _PP, _P]),
     ("muon_orthogonalize_full", _I32, [_P, _P, _P, _P, _I32, _P]),
@@ -276,6 +279,37 @@ def muon_assign_owners(layout, ns_steps=5):
     cost = (ctypes.c_double * max(1, layout.n_shards))()
     _check(lib.muon_assign_owners(layout.handle, int(ns_steps), owner, cost), "muon_assign_owners")
     return [owner[i] for i in range(len(layout.shapes))], [cost[s] for s in range(layout.n_shards)]
+
+
+class Xfer(ctypes.Structure):
+    """muon_xfer: one run of a matrix's flat elements moved between a shard and its
+    owner's packed buffer."""
+    _fields_ = [("param", ctypes.c_int32), ("src_rank", ctypes.c_int32),
+                ("dst_rank", ctypes.c_int32), ("pad_", ctypes.c_int32),
+                ("shard_off", ctypes.c_int64), ("owner_off", ctypes.c_int64),
+                ("len", ctypes.c_int64)]
+
+
+def muon_exchange_plan(layout, owner, rank):
+    """(sends, recvs, owned_numel, owned_offsets) of the owner exchange for `rank`: sends
+    and recvs are lists of dicts with the muon_xfer fields."""
+    n = len(layout.shapes)
+    own = (_I32 * max(1, n))(*[int(o) for o in owner])
+    ns, nr, owned = _I64(0), _I64(0), _I64(0)
+    _check(lib.muon_exchange_plan(layout.handle, own, int(rank), None, ctypes.byref(ns), None,
+                                  ctypes.byref(nr), ctypes.byref(owned), None),
+           "muon_exchange_plan")
+    snd = (Xfer * max(1, ns.value))()
+    rcv = (Xfer * max(1, nr.value))()
+    offs = (_I64 * max(1, n))()
+    _check(lib.muon_exchange_plan(layout.handle, own, int(rank), snd, ctypes.byref(ns), rcv,
+                                  ctypes.byref(nr), ctypes.byref(owned), offs),
+           "muon_exchange_plan")
+
+    def rows(arr, k):
+        return [{f: getattr(arr[i], f) for f, _ in Xfer._fields_ if f != "pad_"}
+                for i in range(k)]
+    return rows(snd, ns.value), rows(rcv, nr.value), owned.value, [offs[i] for i in range(n)]
 
 
 def muon_gather_full(layout, shards, full, stream=None):

@@ -536,6 +536,47 @@ muon_status muon_assign_owners(const muon_layout* layout, int32_t ns_steps, int3
   return ok();
 }
 
+muon_status muon_exchange_plan(const muon_layout* layout, const int32_t* owner, int32_t rank,
+                               muon_xfer* sends, int64_t* n_sends, muon_xfer* recvs,
+                               int64_t* n_recvs, int64_t* owned_numel, int64_t* owned_offsets) {
+  static_assert(sizeof(muon_xfer) == sizeof(XferRun), "muon_xfer and XferRun must agree");
+  if (layout == nullptr) return fail(MUON_ERR_INVALID_ARG, "layout is NULL");
+  const Plan& plan = layout->plan;
+  if (owner == nullptr && plan.n_params > 0) return fail(MUON_ERR_INVALID_ARG, "owner is NULL");
+  if (rank < 0 || rank >= plan.n_shards)
+    return fail(MUON_ERR_INVALID_ARG, "rank=%d outside 0..%d", rank, plan.n_shards - 1);
+  if (n_sends == nullptr || n_recvs == nullptr)
+    return fail(MUON_ERR_INVALID_ARG, "n_sends and n_recvs must not be NULL");
+  std::vector<XferRun> runs;
+  std::vector<int64_t> offs, owned;
+  const std::string err = exchange_runs(plan, owner, &runs, &offs, &owned);
+  if (!err.empty()) return fail(MUON_ERR_INVALID_ARG, "%s", err.c_str());
+  std::vector<XferRun> snd, rcv;
+  for (const XferRun& r : runs) {
+    if (r.src_rank == rank) snd.push_back(r);
+    if (r.dst_rank == rank) rcv.push_back(r);
+  }
+  // runs come in (parameter, offset) order; a stable sort by peer keeps it within a peer
+  std::stable_sort(snd.begin(), snd.end(),
+                   [](const XferRun& a, const XferRun& b) { return a.dst_rank < b.dst_rank; });
+  std::stable_sort(rcv.begin(), rcv.end(),
+                   [](const XferRun& a, const XferRun& b) { return a.src_rank < b.src_rank; });
+  if (sends != nullptr && *n_sends < (int64_t)snd.size())
+    return fail(MUON_ERR_INVALID_ARG, "sends holds %lld runs, %zu needed", (long long)*n_sends,
+                snd.size());
+  if (recvs != nullptr && *n_recvs < (int64_t)rcv.size())
+    return fail(MUON_ERR_INVALID_ARG, "recvs holds %lld runs, %zu needed", (long long)*n_recvs,
+                rcv.size());
+  if (sends != nullptr) std::memcpy(sends, snd.data(), snd.size() * sizeof(XferRun));
+  if (recvs != nullptr) std::memcpy(recvs, rcv.data(), rcv.size() * sizeof(XferRun));
+  *n_sends = (int64_t)snd.size();
+  *n_recvs = (int64_t)rcv.size();
+  if (owned_numel != nullptr) *owned_numel = owned[rank];
+  if (owned_offsets != nullptr)
+    for (int32_t i = 0; i < plan.n_params; ++i) owned_offsets[i] = offs[i];
+  return ok();
+}
+
 muon_status muon_step_grouped(float* const* flat_params, const float* const* flat_grads,
                               float* const* flat_momentum, const muon_layout* layout,
                               void* workspace, const muon_group_hparams* groups, int32_t ns_steps,

@@ -246,6 +246,43 @@ void assign_owners(const Plan& plan, int ns_steps, int32_t* owner, double* rank_
     for (int s = 0; s < S; ++s) rank_cost[s] = load[s];
 }
 
+std::string exchange_runs(const Plan& plan, const int32_t* owner, std::vector<XferRun>* runs,
+                          std::vector<int64_t>* owner_offsets, std::vector<int64_t>* owned_numel) {
+  const int S = plan.n_shards;
+  runs->clear();
+  owner_offsets->assign(plan.n_params, -1);
+  owned_numel->assign(S, 0);
+  for (int32_t i = 0; i < plan.n_params; ++i) {
+    if (!plan.is_matrix[i]) continue;
+    const int32_t o = owner[i];
+    if (o < 0 || o >= S)
+      return fmt("owner[%lld]=%lld outside 0..%lld", i, o, S - 1);
+    // The owner's packed buffer: its parameters in order, each at a multiple of 4.
+    int64_t& end = (*owned_numel)[o];
+    end = round_up(end, 4);
+    (*owner_offsets)[i] = end;
+    const int64_t numel = plan.rows[i] * plan.cols[i];
+    // Cut [flat_off, flat_off + numel) at shard edges.
+    int64_t g = plan.flat_off[i];
+    const int64_t g_end = g + numel;
+    while (g < g_end) {
+      const int64_t s = g / plan.L;
+      const int64_t edge = std::min(g_end, (s + 1) * plan.L);
+      XferRun r{};
+      r.param = i;
+      r.src_rank = (int32_t)s;
+      r.dst_rank = o;
+      r.shard_off = g - s * plan.L;
+      r.owner_off = end + (g - plan.flat_off[i]);
+      r.len = edge - g;
+      runs->push_back(r);
+      g = edge;
+    }
+    end += numel;
+  }
+  return "";
+}
+
 int64_t tile_makespan(const TileList& tl, int phase, int per_tile_units) {
   int64_t worst = 0;
   const int64_t epi = phase == kPhaseUpdate ? 2 : 3;

@@ -122,6 +122,27 @@ TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_s
 // rank_cost[r] receives each rank's total cost in flops for ns_steps iterations.
 void assign_owners(const Plan& plan, int ns_steps, int32_t* owner, double* rank_cost);
 
+// One run of consecutive flat elements of one matrix parameter that the owner exchange
+// moves between a rank's shard and the owner's packed buffer (same layout as muon_xfer).
+struct XferRun {
+  int32_t param;
+  int32_t src_rank;   // rank (= shard index) whose shard holds the run
+  int32_t dst_rank;   // the parameter's owner
+  int32_t pad_;
+  int64_t shard_off;  // element offset of the run in src_rank's shard
+  int64_t owner_off;  // element offset of the run in dst_rank's packed buffer
+  int64_t len;        // elements
+};
+
+// The owner exchange of every matrix parameter (owner[i] in 0..n_shards-1 for matrices):
+// each parameter's flat range cut at shard edges into runs.  owner_offsets[i] (n_params
+// entries) receives parameter i's offset in its owner's packed buffer (the parameters a
+// rank owns, row-major, back to back in parameter order, each starting at a multiple of
+// 4 elements), -1 for non-matrix parameters; owned_numel[r] (n_shards entries) the length
+// of rank r's packed buffer.  Returns "" or a message (an owner out of range).
+std::string exchange_runs(const Plan& plan, const int32_t* owner, std::vector<XferRun>* runs,
+                          std::vector<int64_t>* owner_offsets, std::vector<int64_t>* owned_numel);
+
 // Largest per-CTA load of a tile list, in the cost units plan_tiles balances
 // (k-blocks of 128 x 256 x 64 MMA work plus an epilogue allowance per tile).
 int64_t tile_makespan(const TileList& tl, int phase, int per_tile_units);
