@@ -166,11 +166,14 @@ muon_status muon_apply_local_updates(float* const* flat_params, const muon_layou
                                      void* workspace, float lr, float wd, int32_t ns_steps,
                                      cudaStream_t stream);
 
-/* Stages 2 and 3 in one call (what muon_step runs after stage 1).  On a bf16 layout with
- * ns_steps >= 1 the last Newton-Schulz Update applies W <- W*(1 - lr*wd) - lr*scale*O in
- * its epilogue, from the fp32 O before it is rounded to bf16, and the separate apply pass
- * is skipped; otherwise it equals muon_orthogonalize_updates + muon_apply_local_updates.
- * The bf16 O is still stored, so muon_export_update stays valid. */
+/* Stages 2 and 3 in one call (what muon_step runs after stage 1).  On a tensor-core layout
+ * (bf16 or split fp32) with ns_steps >= 1 whose Newton-Schulz iteration carries at least
+ * 20 TFLOP (3 m^2 n + m^3 per matrix), the last Update applies
+ * W <- W*(1 - lr*wd) - lr*scale*O in its epilogue, from the fp32 O before it is rounded,
+ * and the separate apply pass is skipped (the fused tail); otherwise it equals
+ * muon_orthogonalize_updates + muon_apply_local_updates.  The environment variable
+ * MUON_FUSED_TAIL=1 or 0, read when the layout's tables are prepared, pins the choice.
+ * The rounded O is stored either way, so muon_export_update stays valid. */
 muon_status muon_orthogonalize_apply(float* const* flat_params, const muon_layout* layout,
                                      void* workspace, float lr, float wd, int32_t ns_steps,
                                      cudaStream_t stream);

@@ -192,6 +192,15 @@ muon_status ensure_device(muon_layout* L) {
     t.tc_persistent = false;
     const char* pv = split ? nullptr : std::getenv("MUON_NS_PERSISTENT");  // "1"/"0" pins it
     if (pv != nullptr && (pv[0] == '0' || pv[0] == '1')) t.tc_persistent = pv[0] == '1';
+    // Where the update is applied to W.  On long steps the last Update's epilogue does it
+    // (fused tail): its reductions are long, so the weight traffic hides under the MMAs
+    // and one pass over W and O is saved (Llama-3-8B set: 6-7 ms of a 359 ms step).  Short
+    // reductions make the epilogue the bottleneck, and there the streaming apply kernel
+    // after the last Update is cheaper (GPT-2-small: the fused tail cost 470 us of a
+    // 2.06 ms step, a separate pass over W and O about 130 us).
+    t.fused_tail = all >= kLongStepFlops;
+    const char* fv = std::getenv("MUON_FUSED_TAIL");  // "1"/"0" pins it
+    if (fv != nullptr && (fv[0] == '0' || fv[0] == '1')) t.fused_tail = fv[0] == '1';
     for (MatDev& m : L->plan.mats) m.sig[0] = m.sig[1] = m.sig[2] = 0;
     for (int p = 0; p < 3; ++p) {
       TileList tl = cluster ? plan_tiles(L->plan, p, 256, 256, kTcBK, t.tc_units, !t.tc_persistent)
@@ -312,9 +321,10 @@ muon_status run_ns(muon_layout* L, void* ws, int ns_steps, const ApplyArgs* ap, 
   return MUON_OK;
 }
 
-// Stages 2 and 3.  On the tensor-core path with at least one iteration the last Update's
-// epilogue applies W <- W*(1 - lr*wd) - lr*scale*O itself, from the fp32 O, and the
-// separate apply pass is skipped.
+// Stages 2 and 3.  On the tensor-core paths with at least one iteration and a fused tail
+// (long steps, or MUON_FUSED_TAIL=1) the last Update's epilogue applies
+// W <- W*(1 - lr*wd) - lr*scale*O itself, from the fp32 O, and the separate apply pass
+// is skipped.
 muon_status run_ns_apply(muon_layout* L, const ShardPtrs& w, void* ws, const GroupParams& gp,
                          int ns_steps, cudaStream_t st);
 
@@ -327,7 +337,7 @@ muon_status run_apply(muon_layout* L, const ShardPtrs& w, void* ws, const GroupP
 
 muon_status run_ns_apply(muon_layout* L, const ShardPtrs& w, void* ws, const GroupParams& gp,
                          int ns_steps, cudaStream_t st) {
-  if (L->plan.ns_dtype != MUON_NS_FP32 && ns_steps >= 1) {
+  if (L->plan.ns_dtype != MUON_NS_FP32 && ns_steps >= 1 && L->dt.fused_tail) {
     ApplyArgs ap;
     ap.W = w;
     ap.L = L->plan.L;

@@ -3,9 +3,16 @@
 // of them in one persistent, cooperative launch.
 //
 // Phases of one iteration (quintic Newton-Schulz, (a, b, c) = (3.4445, -4.7750, 2.0315)):
-//   Gram    A = X X^T           (tall X: A = X^T X)      upper-triangle tiles, mirrored
-//   Poly    B = b*A + c*A A     (A symmetric)            upper-triangle tiles, mirrored
-//   Update  X' = s*(a*X + B X)  (tall X: X' = s*(a*X + X B))
+//   Gram    A = X X^T             (tall X: A = X^T X)      upper-triangle tiles, mirrored
+//   Poly    B' = b*A + c*A A + a*I (A symmetric)           upper-triangle tiles, mirrored
+//   Update  X' = s * B' X         (tall X: X' = s * X B')
+// (split fp32: Poly B = b*A + c*A A, Update X' = s*(a*X + B X))
+// a*X + B X = (a*I + B) X, so on the bf16 path the Poly epilogue adds a to the diagonal of
+// B and the Update is a plain product: its epilogue reads no X.  (In bf16 the diagonal
+// entries a + B_ii round to 8 significant bits; on the tested shapes this raises the
+// update's error by 5-10 % of itself, e.g. 0.0095 to 0.0105 on 768 x 2304, within the
+// 2e-2 bound.)  The split-fp32 form keeps a*X + B X: with the large diagonal inside the
+// product, its full-size error rose from 6e-5 to 2e-4, over its 1e-4 bound.
 // s = 1/||X||_F in the first iteration (the Gram epilogue takes s^2), 1 after it.  X keeps
 // its stored row-major orientation; a tall matrix's transposes are MN-major operand reads.
 // The last Update can also apply W <- W*(1 - lr*wd) - lr*sqrt(max(1, r/c))*O from the fp32 O.
@@ -202,17 +209,13 @@ __device__ __forceinline__ void unpack_bf16x32(const uint4 (&u)[4], float (&f)[3
   }
 }
 
-// The global input an epilogue chunk needs besides the accumulator (X for Update, A for
-// Poly), loaded one chunk ahead so that its memory latency overlaps the previous chunk.
+// The global input an epilogue chunk needs besides the accumulator (A, for Poly only),
+// loaded one chunk ahead so that its memory latency overlaps the previous chunk.
 // Returns false when the chunk needs none or takes the element-by-element path.
 __device__ __forceinline__ bool epilogue_prefetch(const NsParams& p, const MatDev& mt, int phase,
-                                                  int x_in, int i, int jb, uint4 (&in)[4]) {
+                                                  int i, int jb, uint4 (&in)[4]) {
   const uint4* src;
-  if (phase == kPhaseUpdate) {
-    if (i >= mt.rows || jb + 32 > mt.cols) return false;
-    src = reinterpret_cast<const uint4*>(p.ws + (x_in ? mt.x1 : mt.x0) +
-                                         2 * ((int64_t)i * mt.ldx + jb));
-  } else if (phase == kPhasePoly) {
+  if (phase == kPhasePoly) {
     if (i >= mt.m || jb + 32 > mt.m || jb + 31 < i) return false;
     src = reinterpret_cast<const uint4*>(p.ws + mt.a + 2 * ((int64_t)i * mt.lda + jb));
   } else {
@@ -237,7 +240,7 @@ __device__ __forceinline__ uint32_t swz64(int r, int c) {
 }
 
 // Epilogue of the 32 x 32 block: rows r0 .. r0+31 (lane = row - r0), accumulator columns
-// [jb, jb+32).  `in` holds the prefetched X or A row segment when have_in.  Full blocks
+// [jb, jb+32).  `in` holds the prefetched A row segment (Poly) when have_in.  Full blocks
 // leave through TMA bulk stores (direct block, and its mirror for the symmetric outputs);
 // blocks on the diagonal of a symmetric output keep the element rule (j >= i written,
 // j > i mirrored) so that every element has exactly one writer.
@@ -253,28 +256,18 @@ __device__ __forceinline__ void epilogue_block(const NsParams& p, const MatDev& 
   bool mirror = false;
   if (phase == kPhaseUpdate) {
     if (r0 >= mt.rows || jb >= mt.cols) return;  // warp-uniform
-    const __nv_bfloat16* xin = reinterpret_cast<const __nv_bfloat16*>(p.ws + (x_in ? mt.x1 : mt.x0));
-    const int64_t row = (int64_t)i * mt.ldx;
-    float x[32];
-    if (have_in) {
-      unpack_bf16x32(in, x);
-    } else {
-#pragma unroll
-      for (int t = 0; t < 32; ++t)
-        x[t] = (i < mt.rows && jb + t < mt.cols) ? __bfloat162float(xin[row + jb + t]) : 0.f;
-    }
     if (apply && i < mt.rows) {
       // Issue the weight loads before any store so that the round trips overlap.
       float w[32];
       const int n = min(32, mt.cols - jb);
       const bool vec = n == 32 && apply_load_row_run(p.ap, mt, i, jb, w);
 #pragma unroll
-      for (int t = 0; t < 32; ++t) f[t] = s * fmaf(kA, x[t], __uint_as_float(acc[t]));
+      for (int t = 0; t < 32; ++t) f[t] = s * __uint_as_float(acc[t]);
       if (vec) apply_store_row_run(p.ap, mt, i, jb, true, w, f);
       else apply_row_run(p.ap, mt, i, jb, n, f);
     } else {
 #pragma unroll
-      for (int t = 0; t < 32; ++t) f[t] = s * fmaf(kA, x[t], __uint_as_float(acc[t]));
+      for (int t = 0; t < 32; ++t) f[t] = s * __uint_as_float(acc[t]);
     }
     out_map = maps + (x_in ? kMapX0St : kMapX1St);
   } else {
@@ -297,13 +290,14 @@ __device__ __forceinline__ void epilogue_block(const NsParams& p, const MatDev& 
       for (int t = 0; t < 32; ++t) f[t] = fmaf(kB, a[t], kC * __uint_as_float(acc[t]));
     }
     if (jb == r0) {
-      // Diagonal block: element rule with plain stores.
+      // Diagonal block: element rule with plain stores; Poly adds a on the diagonal.
       __nv_bfloat16* out = phase == kPhaseGram ? am : reinterpret_cast<__nv_bfloat16*>(p.ws + mt.b);
+      const float diag = phase == kPhasePoly ? kA : 0.f;
       if (i < mt.m) {
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
           const int j = jb + t;
-          if (j >= i && j < mt.m) out[row + j] = __float2bfloat16_rn(f[t]);
+          if (j >= i && j < mt.m) out[row + j] = __float2bfloat16_rn(j == i ? f[t] + diag : f[t]);
           if (j > i && j < mt.m) out[(int64_t)j * mt.lda + i] = __float2bfloat16_rn(f[t]);
         }
       }
@@ -813,7 +807,7 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
             uint4 in_next[4];
             bool have_next = false;
             if constexpr (kVar == kVarTma)
-              have_next = epilogue_prefetch(p, mt, phase, x_in, i, tile.j0 + 32 * c_first, in_next);
+              have_next = epilogue_prefetch(p, mt, phase, i, tile.j0 + 32 * c_first, in_next);
 #pragma unroll 1
             for (int c = c_first; c < c_last; ++c) {
               uint32_t v[32];
@@ -829,8 +823,7 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
                 for (int k = 0; k < 4; ++k) in_cur[k] = in_next[k];
                 const bool have_cur = have_next;
                 if (c + 1 < c_last)
-                  have_next = epilogue_prefetch(p, mt, phase, x_in, i, tile.j0 + 32 * (c + 1),
-                                                in_next);
+                  have_next = epilogue_prefetch(p, mt, phase, i, tile.j0 + 32 * (c + 1), in_next);
                 tmem_ld_32x32b_x32(
                     tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * BN + 32 * c), v);
                 tmem_ld_wait();

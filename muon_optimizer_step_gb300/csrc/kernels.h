@@ -34,6 +34,7 @@ struct DevTables {
   CUtensorMap* tmaps = nullptr; // kMapsPerMat per matrix (bf16 path)
   int tc_shape = kShapeSingle;  // bf16 path: tile shape (kShape*)
   bool tc_persistent = false;   // bf16 path: all phases in one launch (tiles in matrix order)
+  bool fused_tail = false;      // tensor-core paths: the last Update applies W itself
   int tc_units = 0;             // bf16 path: CTAs (or pairs) of each launch; every
                                 // phase's cta_begin has tc_units + 1 entries
   const void* tmap_ws = nullptr;  // workspace the tensor maps were encoded for

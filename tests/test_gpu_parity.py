@@ -527,6 +527,7 @@ def test_fused_tail_each_variant(capi, variant, persistent, monkeypatch):
     rounding of O (2^-8 of each element, times lr * scale)."""
     monkeypatch.setenv("MUON_TC_KERNEL", variant)
     monkeypatch.setenv("MUON_NS_PERSISTENT", persistent)
+    monkeypatch.setenv("MUON_FUSED_TAIL", "1")  # small sets default to the separate apply
     shapes = [(300, 200), (37, 1), (600, 1100), (520, 130), (1, 50)]
     flags = (True, False, True, True, True)
     wl = inputs.Workload("mixed_tail", tuple(shapes), flags, 2, seed=11, rank=4)
