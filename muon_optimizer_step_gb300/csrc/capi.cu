@@ -31,6 +31,8 @@ constexpr long long kDefaultBudget = 4000000000LL;  // ~2 s of SM clock per wait
 // as a long step that runs at the power limit, and the tile shape such buffers get.
 constexpr double kLongStepFlops = 20e12;
 constexpr int kLongStepShape = kShapeSingle;
+// Newton-Schulz work of one iteration below which a buffer runs as one persistent launch.
+constexpr double kPersistentFlops = 1e12;
 constexpr int kMaxDevices = 64;
 int* g_err_word[kMaxDevices] = {nullptr};
 std::mutex g_err_mu;
@@ -183,13 +185,14 @@ muon_status ensure_device(muon_layout* L) {
     const bool cluster = shape != kShapeSingle;
     t.tc_shape = shape;
     t.tc_units = cluster ? pairs : singles;
-    // One launch per phase, each phase's tiles balanced on their own.  The persistent
-    // launch (every phase in one launch, tiles waiting on per-matrix counters) measured
-    // slower on every set: GPT-2-small 2.15 against 2.10 ms, MoE 20.5 against 16.6 ms,
-    // Llama-3-8B about twice as long; it stays available for measurements.  The split-fp32
+    // One launch per phase, each phase's tiles balanced on their own, except for tiny
+    // buffers: there fixed costs per launch weigh most, and the persistent launch (every
+    // phase in one launch, tiles waiting on per-matrix counters) measured faster on
+    // GPT-2-small with CTA pairs (1.487 against 1.572 ms per step) but slower on MoE
+    // (15.7 against 14.8 ms) and two Llama layers (22.9 against 20.1 ms).  The split-fp32
     // epilogue writes with plain stores, which the persistent launch's counters do not
     // publish to the next phase's TMA reads, so it never runs persistent.
-    t.tc_persistent = false;
+    t.tc_persistent = !split && all < kPersistentFlops;
     const char* pv = split ? nullptr : std::getenv("MUON_NS_PERSISTENT");  // "1"/"0" pins it
     if (pv != nullptr && (pv[0] == '0' || pv[0] == '1')) t.tc_persistent = pv[0] == '1';
     // Where the update is applied to W.  On long steps the last Update's epilogue does it

@@ -498,7 +498,8 @@ def test_smoke_entry_point(capi):
 def test_default_kernel_choice(capi, monkeypatch):
     """CTA pairs for two Llama-3-8B layers and for the GPT-2-small set; single CTAs for
     the 32-layer set (94 TFLOP per iteration: long enough to run at the power limit); one
-    launch per phase everywhere; nothing on the fp32 path; an unknown pin is an error."""
+    launch per phase, except GPT-2-small (0.22 TFLOP per iteration: one persistent
+    launch); nothing on the fp32 path; an unknown pin is an error."""
     monkeypatch.delenv("MUON_TC_KERNEL", raising=False)
     monkeypatch.delenv("MUON_NS_PERSISTENT", raising=False)
 
@@ -511,6 +512,8 @@ def test_default_kernel_choice(capi, monkeypatch):
     k = choice("llama3_8b_x32")
     assert k["tile_shape"] == 1 and not k["persistent"] and k["units"] >= 1, k
     k = choice("gpt2_small_x12")
+    assert k["tile_shape"] == 2 and k["persistent"] and k["units"] >= 1, k
+    k = choice("moe_64e")
     assert k["tile_shape"] == 2 and not k["persistent"] and k["units"] >= 1, k
     assert choice("gpt2_small_x12", 1) == {"tile_shape": 0, "units": 0, "persistent": False}
     monkeypatch.setenv("MUON_TC_KERNEL", "3")
