@@ -65,9 +65,11 @@ def elementwise_bytes(n_matrix_elems, ns_dtype):
 # with the same kernel shape and scaled by 16 to the 32-layer set.  Valid only for the
 # kernel shape and the sources it was taken with.
 NS_TRAFFIC = {
-    "llama3_8b_x32": {"bytes_per_launch": 16 * (23543323392 + 9060599296) / 15,
-                      "tile_shape": 3,
-                      "sources_sha256": "b6beba92d6e4364e9451989e8e5b1161d2aea47559532dd1a2ef3beff17ad15c"},
+    # single-CTA tiles with the fused tail, as the 32-layer set runs (MUON_TC_KERNEL=1
+    # MUON_FUSED_TAIL=1 on two layers): 19.27 GB read + 8.96 GB written over 15 launches
+    "llama3_8b_x32": {"bytes_per_launch": 16 * (19270096384 + 8958725888) / 15,
+                      "tile_shape": 1,
+                      "sources_sha256": "40d60a09582d41c5436ed0d15810700ed480411ca95048e3ccbf5b2c0a528887"},
 }
 NS_SOURCES = ("gemm_ns.cu", "device_common.cuh", "layout.cpp")
 
