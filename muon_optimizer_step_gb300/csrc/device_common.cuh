@@ -198,6 +198,23 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, uin
                : "memory");
 }
 
+// The same store with an L2 eviction-priority hint (a createpolicy value).
+__device__ __forceinline__ void tma_store_2d_hint(const void* tmap, int x, int y,
+                                                  uint32_t smem_src, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%1, %2}], [%3], %4;" ::"l"(tmap),
+      "r"(x), "r"(y), "r"(smem_src), "l"(policy)
+      : "memory");
+}
+
+// L2 policy: lines written or read under it are the first candidates for eviction.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

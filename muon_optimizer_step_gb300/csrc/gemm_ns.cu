@@ -329,8 +329,11 @@ __device__ __forceinline__ void epilogue_block(const NsParams& p, const MatDev& 
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
-    tma_store_2d(out_map, jb, r0, smem_u32(st.dir));
-    if (mirror) tma_store_2d(out_map, r0, jb, smem_u32(st.mir));
+    // Outputs are read again only by the next phase: store them evict-first, so that
+    // they do not push out the operand panels this phase's tiles are still streaming.
+    const uint64_t pol = l2_policy_evict_first();
+    tma_store_2d_hint(out_map, jb, r0, smem_u32(st.dir), pol);
+    if (mirror) tma_store_2d_hint(out_map, r0, jb, smem_u32(st.mir), pol);
     bulk_commit();
   }
   st.pending = true;
