@@ -109,6 +109,7 @@ def ns_traffic(workload, ns_dtype, kernel):
 NS_KERNEL_NAMES = {
     1: "ns_tc_single_kernel (tcgen05 cta_group::1, 128x256 tiles)",
     2: "ns_tc_pair_kernel (tcgen05 cta_group::2, 256x256 tiles)",
+    3: "ns_tc_pairwide_kernel (tcgen05 cta_group::2, 256x512 tiles)",
 }
 
 

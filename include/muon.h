@@ -294,8 +294,10 @@ int32_t muon_abi_version(void);
  * device tables there first if no call has (as the first step would).  The pages have no
  * counterpart: it reports a choice this library makes, for tests and measurements.
  * *tile_shape: 1 = one CTA per 128 x 256 tile (tcgen05 cta_group::1); 2 = a 2-CTA cluster
- * per 256 x 256 tile (cta_group::2).  The environment variable MUON_TC_KERNEL=1 or 2 pins
- * the shape for layouts prepared afterwards (any other value: MUON_ERR_INVALID_ARG).
+ * per 256 x 256 tile (cta_group::2); 3 = a 2-CTA cluster per 256 x 512 tile (two
+ * cta_group::2 MMAs of N = 256 per k-step).  The environment variable MUON_TC_KERNEL=1, 2
+ * or 3 pins the shape for layouts prepared afterwards (any other value:
+ * MUON_ERR_INVALID_ARG).
  * *units: CTAs (shape 1) or clusters per launch.  *persistent = 1: all phases of all
  * iterations in one launch; 0: one launch per phase.  All three are 0 on fp32 layouts and
  * layouts without matrices.  MUON_ERR_UNSUPPORTED if the device is not sm_103, or the

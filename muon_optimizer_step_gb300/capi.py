@@ -372,7 +372,7 @@ def muon_selftest_device_check(stream=None):
 
 def muon_layout_ns_kernel(layout) -> dict:
     """The Newton-Schulz kernel `layout` runs on the current device:
-    {"tile_shape": 1 single CTA | 2 CTA pair (0: none),
+    {"tile_shape": 1 single CTA | 2 CTA pair | 3 CTA pair with 256x512 tiles (0: none),
      "units": int, "persistent": bool}."""
     shape, units, pers = _I32(), _I32(), _I32()
     _check(lib.muon_layout_ns_kernel(layout.handle, ctypes.byref(shape), ctypes.byref(units),

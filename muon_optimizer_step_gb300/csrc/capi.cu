@@ -33,6 +33,9 @@ constexpr double kLongStepFlops = 20e12;
 constexpr int kLongStepShape = kShapeSingle;
 // Newton-Schulz work of one iteration below which a buffer runs as one persistent launch.
 constexpr double kPersistentFlops = 1e12;
+// Flop-weighted mean of m (the reduction length of Poly and Update) from which a buffer
+// below the long-step cut runs 256 x 512 CTA-pair tiles.
+constexpr double kWideTileMeanM = 3072.0;
 constexpr int kMaxDevices = 64;
 int* g_err_word[kMaxDevices] = {nullptr};
 std::mutex g_err_mu;
@@ -145,20 +148,29 @@ muon_status ensure_device(muon_layout* L) {
       free_tables(&t);
       return fail(MUON_ERR_UNSUPPORTED, "the tcgen05 kernel does not fit on an SM of device %d", dev);
     }
-    // Two tile shapes, measured on GB300 (bench, bf16):
-    //  - CTA pairs (cta_group::2, 256 x 256 tiles) keep the tensor pipe busiest per clock
-    //    (74-76% of active cycles against 71% for single CTAs on two Llama-3-8B layers) and
-    //    are 2-6% faster wherever the clock stays high: GPT-2, MoE, two Llama layers.
+    // Three tile shapes, measured on GB300 (bench, bf16, alternating runs in one call):
     //  - Steps long enough to hold the GPU at its 1.4 kW limit (the 32-layer Llama-3-8B
-    //    set) are decided by energy per flop instead; there single CTAs hold a higher clock
-    //    than pairs (~1740 against ~1600 MHz) and finish first.
-    // The cut between the two regimes is the Newton-Schulz work of one iteration: 94 TFLOP
-    // on the 32-layer set, 6 on the two-layer one.
-    double all = 0.0;  // flops of one iteration, symmetric count: 3 m^2 n + m^3 per matrix
-    for (const MatDev& m : L->plan.mats)
-      all += 3.0 * m.m * (double)m.m * m.n + (double)m.m * m.m * m.m;
-    int shape = pairs < 1 ? kShapeSingle : (all < kLongStepFlops ? kShapePair : kLongStepShape);
-    const char* v = split ? nullptr : std::getenv("MUON_TC_KERNEL");  // "1" or "2" pins a shape
+    //    set) are decided by energy per flop: single CTAs hold the highest clock and
+    //    finish first (346 ms against 351 for 256 x 512 pair tiles and 353 for pairs).
+    //  - Below the limit the tensor work per clock decides.  With long reductions (two
+    //    Llama layers: flop-weighted mean m of 4000) 256 x 512 pair tiles, with half the
+    //    operand bytes per flop of single CTAs, win: 19.24 against 20.2 ms for pairs and
+    //    20.9 for single CTAs.  With short ones (MoE: m = 1408; GPT-2: m = 768) their
+    //    unoverlapped epilogue costs more than that saves (MoE 16.6 against 14.8 ms), and
+    //    pairs or single CTAs tie.
+    // The cut between the regimes is the Newton-Schulz work of one iteration (94 TFLOP on
+    // the 32-layer set, 6 on the two-layer one) and the flop-weighted mean of m.
+    double all = 0.0, m_sum = 0.0;  // one iteration's flops (3 m^2 n + m^3 per matrix)
+    for (const MatDev& m : L->plan.mats) {
+      const double f = 3.0 * m.m * (double)m.m * m.n + (double)m.m * m.m * m.m;
+      all += f;
+      m_sum += f * m.m;
+    }
+    const double mean_m = all > 0.0 ? m_sum / all : 0.0;
+    int shape = pairs < 1 ? kShapeSingle
+              : all >= kLongStepFlops ? kLongStepShape
+              : mean_m >= kWideTileMeanM ? kShapePairWide : kShapePair;
+    const char* v = split ? nullptr : std::getenv("MUON_TC_KERNEL");  // "1"-"3" pins a shape
     if (split) {
       // The split-fp32 kernel exists for CTA pairs only (two 96 KB operand stages).
       if (pairs < 1) {
@@ -169,10 +181,10 @@ muon_status ensure_device(muon_layout* L) {
       shape = kShapePair;
     }
     if (v != nullptr && v[0] != '\0') {
-      if ((v[0] != '1' && v[0] != '2') || v[1] != '\0') {
+      if (v[0] < '1' || v[0] > '3' || v[1] != '\0') {
         free_tables(&t);
         return fail(MUON_ERR_INVALID_ARG, "MUON_TC_KERNEL=%s: the tile shapes are 1 (single "
-                    "CTA) and 2 (CTA pair)", v);
+                    "CTA), 2 (CTA pair) and 3 (CTA pair, 256 x 512 tiles)", v);
       }
       shape = v[0] - '0';
       if (shape != kShapeSingle && pairs < 1) {
@@ -206,7 +218,8 @@ muon_status ensure_device(muon_layout* L) {
     if (fv != nullptr && (fv[0] == '0' || fv[0] == '1')) t.fused_tail = fv[0] == '1';
     for (MatDev& m : L->plan.mats) m.sig[0] = m.sig[1] = m.sig[2] = 0;
     for (int p = 0; p < 3; ++p) {
-      TileList tl = cluster ? plan_tiles(L->plan, p, 256, 256, kTcBK, t.tc_units, !t.tc_persistent)
+      TileList tl = cluster ? plan_tiles(L->plan, p, 256, shape == kShapePairWide ? 512 : 256,
+                                         kTcBK, t.tc_units, !t.tc_persistent)
                             : plan_tiles(L->plan, p, kTcBM, kTcBN, kTcBK, t.tc_units,
                                          !t.tc_persistent);
       // Every unit of the persistent launch reads begin[unit + 1]: pad the offsets.

@@ -26,13 +26,18 @@
 // phase order and all CTAs are co-resident (cooperative launch, one CTA per SM), so some
 // CTA can always progress; every wait is bounded anyway.
 //
-// Two tile shapes share this code:
+// Three tile shapes share this code:
 //   ns_tc_single_kernel: one CTA per 128 x 256 output tile, tcgen05.mma.cta_group::1, M=128 N=256;
 //   ns_tc_pair_kernel: a 2-CTA cluster per 256 x 256 tile; CTA r loads rows [128r, 128r+128)
 //                  of the A and of the B operand, the even CTA issues
 //                  tcgen05.mma.cta_group::2 (M=256 N=256) over both CTAs' shared memory and
 //                  each CTA drains its own 128 accumulator rows.  A third less operand
-//                  traffic per k-block; used when most of the work sits in big matrices.
+//                  traffic per k-block;
+//   ns_tc_pairwide_kernel: a 2-CTA cluster per 256 x 512 tile: per k-step two such MMAs
+//                  (N = 256 column groups 0 and 1) into one 512-column accumulator; CTA r
+//                  loads its 128 rows of A and 128 rows of each group's B.  Half the
+//                  operand bytes per flop of single CTAs, but the accumulator fills TMEM,
+//                  so a tile's epilogue does not overlap the next tile's MMAs.
 // CTA roles (384 threads): warp 0 (lane 0) issues the TMA loads, warp 1 (lane 0) the MMAs,
 // warp 2 allocates TMEM, warps 4-11 drain TMEM (two warps per TMEM lane quarter warp % 4,
 // half the columns each) through the epilogue.  Registers are split per SM sub-partition:
@@ -72,7 +77,11 @@ template <int kShape, int kVar = kVarTma>
 struct Cfg {
   static constexpr bool kSplit = kVar == kVarSplit;
   static constexpr bool kCluster = kShape != kShapeSingle;  // a 2-CTA cluster per tile
-  static constexpr bool kTwoSm = kShape == kShapePair;      // tcgen05 cta_group::2
+  static constexpr bool kTwoSm = kShape != kShapeSingle;    // tcgen05 cta_group::2
+  static constexpr bool kWide = kShape == kShapePairWide;   // 256 x 512 tiles
+  static constexpr int TILE_N = kWide ? 512 : BN;           // output tile columns
+  static constexpr int ACC_BUFS = kWide ? 1 : 2;  // accumulators in TMEM's 512 columns
+  static constexpr int NHALF = kWide ? 2 : 1;     // N = 256 column groups per k-step
   static constexpr int BK = 64;                       // k-block: one 128-byte row of bf16
   static constexpr int UMMA_K = 16;                   // K of one MMA: 32 bytes of a row
   static constexpr int PARTS = kSplit ? 3 : 1;        // operand copies: h (m, l)
@@ -81,13 +90,14 @@ struct Cfg {
   static constexpr int MMA_M = kTwoSm ? 256 : 128;    // rows of one MMA instruction
   static constexpr int BROWS = kCluster ? 128 : 256;  // B-operand rows this CTA loads
   static constexpr int A_PART = 128 * 128;            // 16 KB: 128 rows of 128 bytes
-  // B rows held in this CTA's stage: its own half (pair), or all 256 (single)
-  static constexpr int B_PART = (kTwoSm ? 128 : 256) * 128;
+  // B rows held in this CTA's stage: its own half of each N = 256 group (pairs), or all
+  // 256 (single)
+  static constexpr int B_PART = (kTwoSm ? 128 * NHALF : 256) * 128;
   static constexpr int A_BYTES = A_PART * PARTS;
   static constexpr int B_BYTES = B_PART * PARTS;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGING = kVar == kVarTma ? EPI_WARPS * 4096 : 0;  // 4 KB per warp
-  static constexpr int STAGES = kTwoSm ? (kSplit ? 2 : 6) : 4;
+  static constexpr int STAGES = kTwoSm ? (kSplit ? 2 : (kWide ? 4 : 6)) : 4;
   static_assert(kVar == kVarTma || kTwoSm, "the plain-store variants run on CTA pairs only");
   // operand stages, epilogue staging, alignment, barriers
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING + 1024 + 256;
@@ -126,7 +136,7 @@ __device__ __forceinline__ bool debug_tiles_ok(const NsParams& p, int unit) {
     if (b0 < 0 || b1 < b0 || b1 > p.n_tiles[phase]) return false;
     for (int ti = b0; ti < b1; ++ti) {
       const TileDev t = p.tiles[phase][ti];
-      if (!debug_tile_ok(t, phase, p.mats, p.dbg, bm, BN, 64)) return false;
+      if (!debug_tile_ok(t, phase, p.mats, p.dbg, bm, Cfg<kShape>::TILE_N, 64)) return false;
       if (p.apply && phase == kPhaseUpdate && !debug_apply_ok(p.ap, p.mats[t.mat], p.dbg))
         return false;
     }
@@ -631,12 +641,17 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
                   } else {
                     tma_load_2d_pair(da, am, k0, ia, fbar);
                   }
-                  if (ops.b_mn) {
 #pragma unroll
-                    for (int q = 0; q < 128 / C::MN_W; ++q)
-                      tma_load_2d_pair(db + q * C::MN_BOX, bm, jr + q * C::MN_W, k0, fbar);
-                  } else {
-                    tma_load_2d_pair(db, bm, k0, jr, fbar);
+                  for (int h = 0; h < C::NHALF; ++h) {  // this CTA's 128 rows of each N group
+                    const uint32_t dbh = db + h * (C::B_PART / C::NHALF);
+                    const int jrh = jr + 256 * h;
+                    if (ops.b_mn) {
+#pragma unroll
+                      for (int q = 0; q < 128 / C::MN_W; ++q)
+                        tma_load_2d_pair(dbh + q * C::MN_BOX, bm, jrh + q * C::MN_W, k0, fbar);
+                    } else {
+                      tma_load_2d_pair(dbh, bm, k0, jrh, fbar);
+                    }
                   }
                 }
               } else {
@@ -701,9 +716,19 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
             const bool idle = !kTwoSm && (row0 >= m_out || (skip_first && skip_second));
             const bool half_n = !idle && (skip_first || skip_second);
             const uint32_t idesc = idesc_bf16(C::MMA_M, half_n ? BN / 2 : BN, ops.a_mn, ops.b_mn);
-            const int ab = lt & 1;
-            if (!wait_role<kCluster>(&acc_empty[ab], (uint32_t)(((lt >> 1) & 1) ^ 1), p, abort,
-                                  peer_abort)) {
+            // 256 x 512 tiles: an N = 256 column group whose outputs the epilogue discards
+            // (all left of the tile's first row in a symmetric phase, or past the matrix)
+            // gets no MMAs.  The decision holds for both CTAs' rows.
+            bool grp_on[C::NHALF];
+#pragma unroll
+            for (int h = 0; h < C::NHALF; ++h) {
+              const int c0 = tile.j0 + 256 * h;
+              grp_on[h] = !C::kWide ||
+                          !(c0 >= n_out || (phase != kPhaseUpdate && c0 + 255 < tile.i0));
+            }
+            const int ab = lt % C::ACC_BUFS;
+            const uint32_t use = (uint32_t)(lt / C::ACC_BUFS);
+            if (!wait_role<kCluster>(&acc_empty[ab], (use & 1u) ^ 1u, p, abort, peer_abort)) {
               ok = false;
               break;
             }
@@ -744,7 +769,13 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
                   tc_mma_f16_pair(d, ad_l, bd, idesc, 1u);
                   tc_mma_f16_pair(d, ad_m, bd_m, idesc, 1u);
                 } else if (kTwoSm) {
-                  tc_mma_f16_pair(d, ad, bd, idesc, acc);
+#pragma unroll
+                  for (int h = 0; h < C::NHALF; ++h) {  // each N = 256 group of a 512-wide tile
+                    if (!grp_on[h]) continue;
+                    const uint64_t bdh = h == 0 ? bd
+                        : smem_desc_sw128(sb + h * (C::B_PART / C::NHALF) + koff_b, lbo_b, 1024);
+                    tc_mma_f16_pair(d + 256u * h, ad, bdh, idesc, acc);
+                  }
                 } else {
                   tc_mma_f16(d, ad, bd, idesc, acc);
                 }
@@ -787,9 +818,10 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
         for (int ti = p.begin[phase][unit]; ti < p.begin[phase][unit + 1]; ++ti, ++lt) {
           const TileDev tile = p.tiles[phase][ti];
           const MatDev& mt = p.mats[tile.mat];
-          const int ab = lt & 1;
-          bool ok = *abort == 0 && mbar_wait_bounded(&acc_full[ab], (uint32_t)((lt >> 1) & 1),
-                                                     p.budget, p.err, abort);
+          const int ab = lt % C::ACC_BUFS;
+          const uint32_t use = (uint32_t)(lt / C::ACC_BUFS);
+          bool ok = *abort == 0 && mbar_wait_bounded(&acc_full[ab], use & 1u, p.budget, p.err,
+                                                     abort);
           ok = __all_sync(0xffffffffu, ok);
           if (ok) {
             tc_fence_after();
@@ -804,7 +836,8 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
             }
             const int r0 = tile.i0 + (kCluster ? 128 * (int)rank : 0) + 32 * q;
             const int i = r0 + lane;
-            const int c_first = half * (BN / 64), c_last = (half + 1) * (BN / 64);
+            // this warp's 32-column blocks: half of the tile's columns
+            const int c_first = half * (C::TILE_N / 64), c_last = (half + 1) * (C::TILE_N / 64);
             // The X (Update) or A (Poly) input of the next 32 x 32 block is loaded before
             // this block's TMEM load and math, so that its memory latency overlaps them.
             uint4 in_next[4];
@@ -889,6 +922,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   ns_tc_body<kShapePair>(p);
 }
 
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    ns_tc_pairwide_kernel(const __grid_constant__ NsParams p) {
+  ns_tc_body<kShapePairWide>(p);
+}
+
 // The split-fp32 form, on CTA pairs.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     ns_tc_split_kernel(const __grid_constant__ NsParams p) {
@@ -899,7 +937,8 @@ using NsKernel = void (*)(NsParams);
 
 template <int kShape>
 NsKernel ns_tc_kernel_of() {
-  return kShape == kShapeSingle ? ns_tc_single_kernel : ns_tc_pair_kernel;
+  return kShape == kShapeSingle ? ns_tc_single_kernel
+         : kShape == kShapePair ? ns_tc_pair_kernel : ns_tc_pairwide_kernel;
 }
 
 __global__ void selftest_timeout_kernel(int* err, long long budget) {
@@ -968,11 +1007,12 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
 }  // namespace
 
 cudaError_t prepare_ns_kernels(int* max_pairs, int* max_singles) {
-  const void* fns[3] = {(const void*)ns_tc_single_kernel, (const void*)ns_tc_pair_kernel,
-                        (const void*)ns_tc_split_kernel};
-  const int smems[3] = {Cfg<kShapeSingle>::SMEM_BYTES, Cfg<kShapePair>::SMEM_BYTES,
-                        Cfg<kShapePair, kVarSplit>::SMEM_BYTES};
-  for (int k = 0; k < 3; ++k) {
+  const void* fns[4] = {(const void*)ns_tc_single_kernel, (const void*)ns_tc_pair_kernel,
+                        (const void*)ns_tc_split_kernel, (const void*)ns_tc_pairwide_kernel};
+  const int smems[4] = {Cfg<kShapeSingle>::SMEM_BYTES, Cfg<kShapePair>::SMEM_BYTES,
+                        Cfg<kShapePair, kVarSplit>::SMEM_BYTES,
+                        Cfg<kShapePairWide>::SMEM_BYTES};
+  for (int k = 0; k < 4; ++k) {
     const void* fn = fns[k];
     const int smem = smems[k];
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -990,13 +1030,14 @@ cudaError_t prepare_ns_kernels(int* max_pairs, int* max_singles) {
   *max_singles = per_sm * sms;
   // Resident 2-CTA clusters: the smallest count of the cluster kernels.
   int n_min = 1 << 30;
-  for (int k = 1; k < 3; ++k) {
+  for (int k = 1; k < 4; ++k) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * 1024, 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smems[k];
     int n = 0;
-    const NsKernel kern = k == 1 ? ns_tc_pair_kernel : ns_tc_split_kernel;
+    const NsKernel kern = k == 1 ? ns_tc_pair_kernel
+                          : k == 2 ? ns_tc_split_kernel : ns_tc_pairwide_kernel;
     e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
     if (e != cudaSuccess) return e;
     n_min = n < n_min ? n : n_min;
@@ -1018,6 +1059,8 @@ cudaError_t launch_ns_tc(const Plan& plan, const DevTables& dt, void* ws, int ns
             ? launch_impl<kShapePair, kVarSplit>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
         : dt.tc_shape == kShapePair
             ? launch_impl<kShapePair>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
+        : dt.tc_shape == kShapePairWide
+            ? launch_impl<kShapePairWide>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st)
             : launch_impl<kShapeSingle>(plan, dt, ws, ns_steps, q0, q0 + step, budget, ap, st);
     if (e != cudaSuccess) return e;
   }

@@ -19,6 +19,8 @@ struct DebugCtx;
 // muon_layout_ns_kernel reports).
 constexpr int kShapeSingle = 1;  // one CTA per 128 x 256 tile, tcgen05 cta_group::1
 constexpr int kShapePair = 2;    // 2-CTA cluster per 256 x 256 tile, tcgen05 cta_group::2
+constexpr int kShapePairWide = 3;  // 2-CTA cluster per 256 x 512 tile: two cta_group::2
+                                   // MMAs of N = 256 per k-step into one 512-column accumulator
 
 // Device-resident tables of a layout (uploaded once per device).
 struct DevTables {

@@ -397,16 +397,16 @@ def test_wait_timeout_is_reported_and_context_survives(capi):
     assert float(x.sum()) == 16.0
 
 
-@pytest.mark.parametrize("variant", ["1", "2"])
+@pytest.mark.parametrize("variant", ["1", "2", "3"])
 @pytest.mark.parametrize("persistent", ["0", "1"])
 def test_each_tcgen05_variant_vs_oracle(capi, variant, persistent, monkeypatch):
-    """The two tcgen05 tile shapes (single CTA 128x256 tiles; 256x256 tiles on CTA pairs)
-    and both launch modes (one launch per phase; one persistent launch whose tiles wait on
+    """The three tcgen05 tile shapes (single CTA 128x256 tiles; 256x256 and 256x512 tiles
+    on CTA pairs) and both launch modes (one launch per phase; one persistent launch whose tiles wait on
     per-matrix counters), pinned one at a time, on ragged shapes and on a matrix that
     spans several pair tiles."""
     monkeypatch.setenv("MUON_TC_KERNEL", variant)
     monkeypatch.setenv("MUON_NS_PERSISTENT", persistent)
-    shapes = [(300, 200), (130, 520), (7, 3), (64, 1000), (257, 129), (600, 1100)]
+    shapes = [(300, 200), (130, 520), (7, 3), (64, 1000), (257, 129), (600, 1100), (1100, 600)]
     wl = inputs.Workload("mixed", tuple(shapes), (True,) * len(shapes), 1, seed=9, rank=4)
     lay = capi.muon_layout_create(wl.shapes, 1, 0, wl.is_matrix)
     k = capi.muon_layout_ns_kernel(lay)
@@ -496,10 +496,11 @@ def test_smoke_entry_point(capi):
 
 
 def test_default_kernel_choice(capi, monkeypatch):
-    """CTA pairs for two Llama-3-8B layers and for the GPT-2-small set; single CTAs for
-    the 32-layer set (94 TFLOP per iteration: long enough to run at the power limit); one
-    launch per phase, except GPT-2-small (0.22 TFLOP per iteration: one persistent
-    launch); nothing on the fp32 path; an unknown pin is an error."""
+    """256 x 512 CTA-pair tiles for two Llama-3-8B layers (long reductions); CTA pairs for
+    the GPT-2-small and MoE sets; single CTAs for the 32-layer set (94 TFLOP per
+    iteration: long enough to run at the power limit); one launch per phase, except
+    GPT-2-small (0.22 TFLOP per iteration: one persistent launch); nothing on the fp32
+    path; an unknown pin is an error."""
     monkeypatch.delenv("MUON_TC_KERNEL", raising=False)
     monkeypatch.delenv("MUON_NS_PERSISTENT", raising=False)
 
@@ -508,7 +509,7 @@ def test_default_kernel_choice(capi, monkeypatch):
         return capi.muon_layout_ns_kernel(capi.muon_layout_create(wl.shapes, 1, dtype,
                                                                   wl.is_matrix))
     k = choice("llama3_8b_x2")
-    assert k["tile_shape"] == 2 and not k["persistent"] and k["units"] >= 1, k
+    assert k["tile_shape"] == 3 and not k["persistent"] and k["units"] >= 1, k
     k = choice("llama3_8b_x32")
     assert k["tile_shape"] == 1 and not k["persistent"] and k["units"] >= 1, k
     k = choice("gpt2_small_x12")
@@ -516,13 +517,13 @@ def test_default_kernel_choice(capi, monkeypatch):
     k = choice("moe_64e")
     assert k["tile_shape"] == 2 and not k["persistent"] and k["units"] >= 1, k
     assert choice("gpt2_small_x12", 1) == {"tile_shape": 0, "units": 0, "persistent": False}
-    monkeypatch.setenv("MUON_TC_KERNEL", "3")
+    monkeypatch.setenv("MUON_TC_KERNEL", "4")
     with pytest.raises(capi.MuonError) as e:
         choice("llama3_8b_x2")
     assert e.value.status == capi.MUON_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("variant", ["1", "2"])
+@pytest.mark.parametrize("variant", ["1", "2", "3"])
 @pytest.mark.parametrize("persistent", ["0", "1"])
 def test_fused_tail_each_variant(capi, variant, persistent, monkeypatch):
     """muon_step (whose last Update applies W) against the three separate stages, for each
