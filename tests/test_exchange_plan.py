@@ -1,9 +1,9 @@
 """The owner exchange plan ("Add initial Muon+M-FSDPv2 implementation", "Opt step" steps 3
 and 5): per rank, the runs of matrix elements sent to owners and received from shard
 holders.  Host only: the library's planner is checked by brute force on tiny layouts, and
-moving the data with torch.distributed on CPU tensors (gloo, 2 and 3 ranks) rebuilds, bit
-for bit, what the oracle's gather gives on each owner and, on the way back, what its
-scatter gives on each shard."""
+moving the data with the package's OwnerExchange (torch.distributed point-to-point on CPU
+tensors: gloo, 2 and 3 ranks) rebuilds, bit for bit, what the oracle's gather gives on
+each owner and, on the way back, what its scatter gives on each shard."""
 import os
 import socket
 import sys
@@ -116,6 +116,7 @@ def _exchange_main(rank, world, port, out_dir):
     import torch.distributed as dist
     from muon_optimizer_step_gb300 import capi as c
     from muon_optimizer_step_gb300 import inputs as inp
+    from muon_optimizer_step_gb300.exchange import OwnerExchange
     from oracle import muon_ref as oref
     dist.init_process_group("gloo", rank=rank, world_size=world)
     # straddling parameters: the ragged set plus a vector, split over `world` shards
@@ -124,60 +125,15 @@ def _exchange_main(rank, world, port, out_dir):
     flags = list(wl.is_matrix) + [False, True]
     lay = c.muon_layout_create(shapes, world, 0, flags)
     owner, _ = c.muon_assign_owners(lay)
-    sends, recvs, owned_numel, offs = c.muon_exchange_plan(lay, owner, rank)
+    ex = OwnerExchange(lay, owner, rank)
     o = oref.flat_layout(shapes, world, flags)
     flat = np.random.default_rng(11).normal(size=lay.numel).astype(np.float32)
-    my_shard = oref.shard_flat(flat, o)[rank].astype(np.float32)
-
-    def move(src_lists, dst_lists, read, write):
-        """One message per peer: the runs to that peer back to back, in list order."""
-        reqs = []
-        for peer in range(world):
-            out = [x for x in src_lists if x["dst_rank" if read == "shard" else "src_rank"] == peer]
-            if not out:
-                continue
-            buf = np.concatenate([read_run(x, read) for x in out]).astype(np.float32)
-            if peer == rank:
-                local[peer] = buf
-            else:
-                reqs.append(dist.isend(torch.from_numpy(buf), dst=peer))
-        for peer in range(world):
-            inc = [x for x in dst_lists if x["src_rank" if read == "shard" else "dst_rank"] == peer]
-            if not inc:
-                continue
-            n = sum(x["len"] for x in inc)
-            if peer == rank:
-                buf = local[peer]
-            else:
-                t = torch.empty(n, dtype=torch.float32)
-                dist.recv(t, src=peer)
-                buf = t.numpy()
-            pos = 0
-            for x in inc:
-                write_run(x, write, buf[pos: pos + x["len"]])
-                pos += x["len"]
-        for q in reqs:
-            q.wait()
-
-    owner_buf = np.full(max(1, owned_numel), np.nan, dtype=np.float32)
-    shard_back = np.full(o["L"], 7.0, dtype=np.float32)
-
-    def read_run(x, where):
-        if where == "shard":
-            return my_shard[x["shard_off"]: x["shard_off"] + x["len"]]
-        return owner_buf[x["owner_off"]: x["owner_off"] + x["len"]]
-
-    def write_run(x, where, vals):
-        if where == "owner":
-            owner_buf[x["owner_off"]: x["owner_off"] + x["len"]] = vals
-        else:
-            shard_back[x["shard_off"]: x["shard_off"] + x["len"]] = vals
-
-    local = {}
+    my_shard = torch.from_numpy(oref.shard_flat(flat, o)[rank].astype(np.float32))
     # step 3: shards -> owners
-    move(sends, recvs, "shard", "owner")
+    owned = ex.gather_to_owners(dist, my_shard).numpy()
     full = oref.gather_full(oref.shard_flat(flat, o), o)
-    ok_gather = all(np.array_equal(owner_buf[offs[i]: offs[i] + full[i].size],
+    offs = ex.owned_offsets
+    ok_gather = all(np.array_equal(owned[offs[i]: offs[i] + full[i].size],
                                    full[i].astype(np.float32).reshape(-1))
                     for i in full if owner[i] == rank)
     # the owner's "updates": a fresh seeded value per owned matrix element
@@ -185,14 +141,14 @@ def _exchange_main(rank, world, port, out_dir):
            for i in full}
     for i in full:
         if owner[i] == rank:
-            owner_buf[offs[i]: offs[i] + full[i].size] = upd[i].reshape(-1)
+            owned[offs[i]: offs[i] + full[i].size] = upd[i].reshape(-1)
     # step 5: owners -> shards (the same runs, reversed)
-    local = {}
-    move(recvs, sends, "owner", "shard")
+    back = torch.full((o["L"],), 7.0, dtype=torch.float32)
+    ex.scatter_from_owners(dist, torch.from_numpy(owned), back)
     want = oref.scatter_updates(upd, o, [np.full(o["L"], 7.0) for _ in range(world)])[rank]
-    ok_scatter = np.array_equal(shard_back, np.asarray(want, dtype=np.float32))
+    ok_scatter = np.array_equal(back.numpy(), np.asarray(want, dtype=np.float32))
     with open(os.path.join(out_dir, f"rank{rank}.txt"), "w") as f:
-        f.write(f"{int(ok_gather)} {int(ok_scatter)} {len(sends)} {len(recvs)}\n")
+        f.write(f"{int(ok_gather)} {int(ok_scatter)} {len(ex.sends)} {len(ex.recvs)}\n")
     dist.barrier()
     dist.destroy_process_group()
 
