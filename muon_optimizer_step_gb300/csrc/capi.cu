@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <algorithm>
+#include <cstdint>
 #include <cstdlib>
 #include <cstdio>
 #include <cstring>
@@ -33,6 +34,8 @@ constexpr double kLongStepFlops = 20e12;
 constexpr int kLongStepShape = kShapeSingle;
 // Newton-Schulz work of one iteration below which a buffer runs as one persistent launch.
 constexpr double kPersistentFlops = 1e12;
+// Iterations with their own tile lists in a persistent launch (later ones reuse the last).
+constexpr int kPersistentIters = 6;
 // Flop-weighted mean of m (the reduction length of Poly and Update) from which a buffer
 // below the long-step cut runs 256 x 512 CTA-pair tiles.
 constexpr double kWideTileMeanM = 3072.0;
@@ -98,6 +101,8 @@ void free_tables(DevTables* dt) {
     cudaFree(dt->tiles[p]);
     cudaFree(dt->cta_begin[p]);
   }
+  cudaFree(dt->tc_tiles);
+  cudaFree(dt->tc_begin);
   cudaFree(dt->tmaps);
   if (cur >= 0 && cur != dt->device) cudaSetDevice(cur);
   *dt = DevTables{};
@@ -217,19 +222,36 @@ muon_status ensure_device(muon_layout* L) {
     const char* fv = std::getenv("MUON_FUSED_TAIL");  // "1"/"0" pins it
     if (fv != nullptr && (fv[0] == '0' || fv[0] == '1')) t.fused_tail = fv[0] == '1';
     for (MatDev& m : L->plan.mats) m.sig[0] = m.sig[1] = m.sig[2] = 0;
-    for (int p = 0; p < 3; ++p) {
-      TileList tl = cluster ? plan_tiles(L->plan, p, 256, shape == kShapePairWide ? 512 : 256,
-                                         kTcBK, t.tc_units, !t.tc_persistent)
-                            : plan_tiles(L->plan, p, kTcBM, kTcBN, kTcBK, t.tc_units,
-                                         !t.tc_persistent);
-      // Every unit of the persistent launch reads begin[unit + 1]: pad the offsets.
-      while ((int)tl.cta_begin.size() < t.tc_units + 1) tl.cta_begin.push_back(tl.cta_begin.back());
-      for (const TileDev& td : tl.tiles) L->plan.mats[td.mat].sig[p] += cluster ? 2 : 1;
-      t.grid[p] = tl.grid;
-      t.n_tiles[p] = (int64_t)tl.tiles.size();
-      if ((s = upload(tl.tiles, &t.tiles[p])) != MUON_OK) { free_tables(&t); return s; }
-      if ((s = upload(tl.cta_begin, &t.cta_begin[p])) != MUON_OK) { free_tables(&t); return s; }
+    const int bm = cluster ? 256 : kTcBM;
+    const int bn = shape == kShapePairWide ? 512 : cluster ? 256 : kTcBN;
+    std::vector<TileList> lists;
+    if (t.tc_persistent) {
+      // Lists per iteration: matrices reach each phase at different times, so the best
+      // order of a phase's tiles differs from one iteration to the next.
+      lists = plan_persistent(L->plan, bm, bn, kTcBK, t.tc_units, kPersistentIters);
+    } else {
+      for (int p = 0; p < 3; ++p) lists.push_back(plan_tiles(L->plan, p, bm, bn, kTcBK, t.tc_units));
     }
+    for (int p = 0; p < 3; ++p)
+      for (const TileDev& td : lists[p].tiles) L->plan.mats[td.mat].sig[p] += cluster ? 2 : 1;
+    // Back to back; every unit of a launch reads begin[unit + 1], so each list's offsets
+    // are padded to tc_units + 1 entries.
+    std::vector<TileDev> all_tiles;
+    std::vector<int32_t> all_begin;
+    for (TileList& tl : lists) {
+      while ((int)tl.cta_begin.size() < t.tc_units + 1) tl.cta_begin.push_back(tl.cta_begin.back());
+      for (int u = 0; u <= t.tc_units; ++u)
+        all_begin.push_back((int32_t)all_tiles.size() + tl.cta_begin[u]);
+      all_tiles.insert(all_tiles.end(), tl.tiles.begin(), tl.tiles.end());
+    }
+    if (all_tiles.size() > (size_t)INT32_MAX) {
+      free_tables(&t);
+      return fail(MUON_ERR_UNSUPPORTED, "more than 2^31 Newton-Schulz tiles");
+    }
+    t.tc_lists = (int)lists.size();
+    t.tc_n_tiles = (int64_t)all_tiles.size();
+    if ((s = upload(all_tiles, &t.tc_tiles)) != MUON_OK) { free_tables(&t); return s; }
+    if ((s = upload(all_begin, &t.tc_begin)) != MUON_OK) { free_tables(&t); return s; }
     e = cudaMalloc(&t.tmaps, L->plan.mats.size() * kMapsPerMat * sizeof(CUtensorMap));
     if (e != cudaSuccess) { free_tables(&t); return fail(MUON_ERR_OOM, "cudaMalloc(tensor maps)"); }
   }

@@ -17,14 +17,17 @@
 // its stored row-major orientation; a tall matrix's transposes are MN-major operand reads.
 // The last Update can also apply W <- W*(1 - lr*wd) - lr*sqrt(max(1, r/c))*O from the fp32 O.
 //
-// Scheduling: the host deals each phase's tiles to CTAs (longest first); a CTA walks its
-// lists for iteration 0..n-1, phase Gram, Poly, Update.  A tile starts when the phase it
+// Scheduling: the host deals the tiles to CTAs, per phase (longest first) when each phase
+// is a launch of its own.  A persistent launch walks, per CTA, one list per iteration and
+// phase (Gram, Poly, Update of iteration 0, then 1, ...).  A tile starts when the phase it
 // reads is complete *for its own matrix*: per matrix and phase a counter in the workspace
 // counts finished CTA-tiles (release after the epilogue's stores; acquire + an async-proxy
 // fence before the TMA reads).  Matrices therefore flow through the phases independently,
-// and the tail of one phase overlaps the start of the next.  Every CTA's lists are in
-// phase order and all CTAs are co-resident (cooperative launch, one CTA per SM), so some
-// CTA can always progress; every wait is bounded anyway.
+// and the tail of one phase overlaps the start of the next; the host orders each list by
+// when its tiles' inputs are expected to be complete (a simulated run).  Every CTA's lists
+// are in phase order and all CTAs are co-resident (cooperative launch, one CTA per SM):
+// the lowest unfinished phase only waits on finished ones, so some CTA can always
+// progress, whatever the order inside a list; every wait is bounded anyway.
 //
 // Three tile shapes share this code:
 //   ns_tc_single_kernel: one CTA per 128 x 256 output tile, tcgen05.mma.cta_group::1, M=128 N=256;
@@ -105,8 +108,10 @@ struct Cfg {
 };
 
 struct NsParams {
-  const TileDev* tiles[3];
-  const int32_t* begin[3];   // per phase: tile-list offsets per CTA (per cluster)
+  const TileDev* tiles;      // every tile list, back to back
+  const int32_t* begin;      // list l, unit u: tiles [begin[l*begin_stride+u], begin[...+u+1])
+  int begin_stride;          // units + 1
+  int n_lists;               // 3 (one per phase) or 3 x iterations (persistent)
   const MatDev* mats;
   const CUtensorMap* tmaps;
   uint8_t* ws;
@@ -118,9 +123,16 @@ struct NsParams {
   int q_begin, q_end;        // this launch runs phases q = 3*it + phase in [q_begin, q_end)
   int apply;                 // last Update also applies the step to W
   ApplyArgs ap;
-  int64_t n_tiles[3];        // entries of each phase's tile list
+  int64_t n_tiles;           // entries of `tiles`
   DebugCtx dbg;
 };
+
+// The offsets of unit `unit` in the tile list of q = 3 * it + phase (its own list, or for
+// iterations past the lists the last iteration's).
+__device__ __forceinline__ const int32_t* list_begin(const NsParams& p, int qq, int unit) {
+  const int l = qq < p.n_lists ? qq : p.n_lists - 3 + qq % 3;
+  return p.begin + (int64_t)l * p.begin_stride + unit;
+}
 
 // Debug builds: every tile this CTA (pair) will run in this launch, checked before any
 // role starts.  The answer depends on the tables only, so both CTAs of a pair reach the
@@ -128,14 +140,14 @@ struct NsParams {
 template <int kShape>
 __device__ __forceinline__ bool debug_tiles_ok(const NsParams& p, int unit) {
   constexpr int bm = kShape == kShapeSingle ? 128 : 256;
-  for (int phase = 0; phase < 3; ++phase) {
-    bool used = false;
-    for (int qq = p.q_begin; qq < p.q_end; ++qq) used |= (qq % 3) == phase;
-    if (!used) continue;
-    const int b0 = p.begin[phase][unit], b1 = p.begin[phase][unit + 1];
-    if (b0 < 0 || b1 < b0 || b1 > p.n_tiles[phase]) return false;
+  if (p.n_lists < 3 || p.n_lists % 3 != 0 || unit + 1 >= p.begin_stride) return false;
+  for (int qq = p.q_begin; qq < p.q_end; ++qq) {
+    const int phase = qq % 3;
+    const int32_t* bg = list_begin(p, qq, unit);
+    const int b0 = bg[0], b1 = bg[1];
+    if (b0 < 0 || b1 < b0 || b1 > p.n_tiles) return false;
     for (int ti = b0; ti < b1; ++ti) {
-      const TileDev t = p.tiles[phase][ti];
+      const TileDev t = p.tiles[ti];
       if (!debug_tile_ok(t, phase, p.mats, p.dbg, bm, Cfg<kShape>::TILE_N, 64)) return false;
       if (p.apply && phase == kPhaseUpdate && !debug_apply_ok(p.ap, p.mats[t.mat], p.dbg))
         return false;
@@ -596,8 +608,9 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
         const int it = qq / 3, phase = qq % 3;
         {
           const int x_in = it & 1;
-          for (int ti = p.begin[phase][unit]; ti < p.begin[phase][unit + 1] && ok; ++ti) {
-            const TileDev tile = p.tiles[phase][ti];
+          const int32_t* bg = list_begin(p, qq, unit);
+          for (int ti = bg[0]; ti < bg[1] && ok; ++ti) {
+            const TileDev tile = p.tiles[ti];
             const MatDev& mt = p.mats[tile.mat];
             int target;
             const int slot = dep_slot(mt, tile.mat, it, phase, &target);
@@ -697,8 +710,9 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
       for (int qq = p.q_begin; qq < p.q_end && ok; ++qq) {
         const int it = qq / 3, phase = qq % 3;
         {
-          for (int ti = p.begin[phase][unit]; ti < p.begin[phase][unit + 1]; ++ti, ++lt) {
-            const TileDev tile = p.tiles[phase][ti];
+          const int32_t* bg = list_begin(p, qq, unit);
+          for (int ti = bg[0]; ti < bg[1]; ++ti, ++lt) {
+            const TileDev tile = p.tiles[ti];
             const MatDev& mt = p.mats[tile.mat];
             const TileOps ops = tile_ops<kCluster>(mt, phase, it & 1);
             // Columns the epilogue would discard are not computed (single CTAs; a pair's
@@ -815,8 +829,9 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
       {
         const int x_in = it & 1;
         const bool apply = p.apply && phase == kPhaseUpdate && it == p.ns_steps - 1;
-        for (int ti = p.begin[phase][unit]; ti < p.begin[phase][unit + 1]; ++ti, ++lt) {
-          const TileDev tile = p.tiles[phase][ti];
+        const int32_t* bg = list_begin(p, qq, unit);
+        for (int ti = bg[0]; ti < bg[1]; ++ti, ++lt) {
+          const TileDev tile = p.tiles[ti];
           const MatDev& mt = p.mats[tile.mat];
           const int ab = lt % C::ACC_BUFS;
           const uint32_t use = (uint32_t)(lt / C::ACC_BUFS);
@@ -960,10 +975,10 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
                         cudaStream_t st) {
   uint8_t* w = static_cast<uint8_t*>(ws);
   NsParams p;
-  for (int ph = 0; ph < 3; ++ph) {
-    p.tiles[ph] = dt.tiles[ph];
-    p.begin[ph] = dt.cta_begin[ph];
-  }
+  p.tiles = dt.tc_tiles;
+  p.begin = dt.tc_begin;
+  p.begin_stride = dt.tc_units + 1;
+  p.n_lists = dt.tc_lists;
   p.mats = dt.mats;
   p.tmaps = dt.tmaps;
   p.ws = w;
@@ -976,7 +991,7 @@ cudaError_t launch_impl(const Plan& plan, const DevTables& dt, void* ws, int ns_
   p.q_end = q_end;
   p.apply = ap != nullptr ? 1 : 0;
   if (ap != nullptr) p.ap = *ap;
-  for (int ph = 0; ph < 3; ++ph) p.n_tiles[ph] = dt.n_tiles[ph];
+  p.n_tiles = dt.tc_n_tiles;
   p.dbg = make_debug_ctx(plan, dt);
   cudaError_t e = cudaSuccess;
   if (q_end - q_begin > 1) {

@@ -29,16 +29,24 @@ struct DevTables {
   ChunkDev* chunks = nullptr;
   MatDev* mats = nullptr;
   int* err = nullptr;           // device error word (MUON_ERR_TIMEOUT when a wait gave up)
+  // fp32 path: one tile list per phase
   TileDev* tiles[3] = {nullptr, nullptr, nullptr};
   int32_t* cta_begin[3] = {nullptr, nullptr, nullptr};
   int64_t n_tiles[3] = {0, 0, 0};  // entries of each phase's tile list
   int grid[3] = {0, 0, 0};
+  // Tensor-core paths: tc_lists tile lists back to back in tc_tiles; list l's offsets for
+  // unit u are tc_begin[l * (tc_units + 1) + u] and the next entry.  One list per phase,
+  // or, for a persistent launch, one per iteration and phase (q = 3 * it + phase), the
+  // last iteration's lists serving any later one.
+  TileDev* tc_tiles = nullptr;
+  int32_t* tc_begin = nullptr;
+  int tc_lists = 0;
+  int64_t tc_n_tiles = 0;
   CUtensorMap* tmaps = nullptr; // kMapsPerMat per matrix (bf16 path)
   int tc_shape = kShapeSingle;  // bf16 path: tile shape (kShape*)
-  bool tc_persistent = false;   // bf16 path: all phases in one launch (tiles in matrix order)
+  bool tc_persistent = false;   // bf16 path: all phases in one launch
   bool fused_tail = false;      // tensor-core paths: the last Update applies W itself
-  int tc_units = 0;             // bf16 path: CTAs (or pairs) of each launch; every
-                                // phase's cta_begin has tc_units + 1 entries
+  int tc_units = 0;             // tensor-core paths: CTAs (or pairs) of each launch
   const void* tmap_ws = nullptr;  // workspace the tensor maps were encoded for
 };
 

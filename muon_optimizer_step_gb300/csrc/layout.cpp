@@ -148,9 +148,15 @@ std::string build_plan(const int64_t* shapes, const uint8_t* is_matrix, int32_t 
   return "";
 }
 
-TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_sms,
-                    bool by_cost) {
-  struct Item { TileDev t; int64_t cost; };
+namespace {
+
+struct Item {
+  TileDev t;
+  int64_t cost;  // k-blocks plus an epilogue allowance
+};
+
+// The output tiles of one phase over every matrix, in matrix order.
+std::vector<Item> phase_items(const Plan& plan, int phase, int bm, int bn, int bk) {
   std::vector<Item> items;
   for (size_t mi = 0; mi < plan.mats.size(); ++mi) {
     const MatDev& m = plan.mats[mi];
@@ -178,32 +184,20 @@ TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_s
         it.t.i0 = i0;
         it.t.j0 = j0;
         it.t.kblocks = kb;
-        it.cost = (int64_t)kb + (sym ? 3 : 2);  // k-blocks plus an epilogue allowance
+        it.cost = (int64_t)kb + (sym ? 3 : 2);
         items.push_back(it);
       }
     }
   }
-  if (by_cost)
-    std::stable_sort(items.begin(), items.end(),
-                     [](const Item& a, const Item& b) { return a.cost > b.cost; });
+  return items;
+}
+
+// Heap of units by the cost-time at which they free up (lowest index on ties).
+using Slot = std::pair<int64_t, int>;
+using SlotHeap = std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>>;
+
+TileList pack_lists(std::vector<std::vector<TileDev>>& per, int grid) {
   TileList tl;
-  if (items.empty() || n_sms <= 0) {
-    tl.grid = 0;
-    tl.cta_begin.assign(1, 0);
-    return tl;
-  }
-  const int grid = (int)std::min<int64_t>((int64_t)items.size(), n_sms);
-  // LPT: each tile, most expensive first, goes to the least-loaded CTA (lowest index on ties).
-  using Slot = std::pair<int64_t, int>;
-  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-  for (int c = 0; c < grid; ++c) heap.push({0, c});
-  std::vector<std::vector<TileDev>> per(grid);
-  for (const Item& it : items) {
-    Slot s = heap.top();
-    heap.pop();
-    per[s.second].push_back(it.t);
-    heap.push({s.first + it.cost, s.second});
-  }
   tl.grid = grid;
   tl.cta_begin.resize(grid + 1);
   tl.cta_begin[0] = 0;
@@ -212,6 +206,69 @@ TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_s
     tl.tiles.insert(tl.tiles.end(), per[c].begin(), per[c].end());
   }
   return tl;
+}
+
+}  // namespace
+
+TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_sms,
+                    bool by_cost) {
+  std::vector<Item> items = phase_items(plan, phase, bm, bn, bk);
+  if (by_cost)
+    std::stable_sort(items.begin(), items.end(),
+                     [](const Item& a, const Item& b) { return a.cost > b.cost; });
+  if (items.empty() || n_sms <= 0) {
+    TileList tl;
+    tl.grid = 0;
+    tl.cta_begin.assign(1, 0);
+    return tl;
+  }
+  const int grid = (int)std::min<int64_t>((int64_t)items.size(), n_sms);
+  // LPT: each tile, most expensive first, goes to the least-loaded CTA (lowest index on ties).
+  SlotHeap heap;
+  for (int c = 0; c < grid; ++c) heap.push({0, c});
+  std::vector<std::vector<TileDev>> per(grid);
+  for (const Item& it : items) {
+    Slot s = heap.top();
+    heap.pop();
+    per[s.second].push_back(it.t);
+    heap.push({s.first + it.cost, s.second});
+  }
+  return pack_lists(per, grid);
+}
+
+std::vector<TileList> plan_persistent(const Plan& plan, int bm, int bn, int bk, int units,
+                                      int iters) {
+  std::vector<TileList> out;
+  if (units <= 0 || iters <= 0) return out;
+  std::vector<Item> items[3];
+  for (int ph = 0; ph < 3; ++ph) items[ph] = phase_items(plan, ph, bm, bn, bk);
+  const size_t nm = plan.mats.size();
+  std::vector<int64_t> ready(nm, 0), done(nm, 0);
+  SlotHeap heap;
+  for (int u = 0; u < units; ++u) heap.push({0, u});
+  for (int q = 0; q < 3 * iters; ++q) {
+    const std::vector<Item>& it = items[q % 3];
+    std::vector<size_t> order(it.size());
+    std::iota(order.begin(), order.end(), size_t{0});
+    std::stable_sort(order.begin(), order.end(), [&](size_t a, size_t b) {
+      const int64_t ra = ready[it[a].t.mat], rb = ready[it[b].t.mat];
+      return ra != rb ? ra < rb : it[a].cost > it[b].cost;
+    });
+    std::vector<std::vector<TileDev>> per(units);
+    std::fill(done.begin(), done.end(), 0);
+    for (size_t k : order) {
+      const Item& x = it[k];
+      const Slot s = heap.top();
+      heap.pop();
+      const int64_t start = std::max(s.first, ready[x.t.mat]);
+      per[s.second].push_back(x.t);
+      done[x.t.mat] = std::max(done[x.t.mat], start + x.cost + kPublishLag);
+      heap.push({start + x.cost, s.second});
+    }
+    ready.swap(done);
+    out.push_back(pack_lists(per, units));
+  }
+  return out;
 }
 
 void assign_owners(const Plan& plan, int ns_steps, int32_t* owner, double* rank_cost) {
@@ -281,18 +338,6 @@ std::string exchange_runs(const Plan& plan, const int32_t* owner, std::vector<Xf
     end += numel;
   }
   return "";
-}
-
-int64_t tile_makespan(const TileList& tl, int phase, int per_tile_units) {
-  int64_t worst = 0;
-  const int64_t epi = phase == kPhaseUpdate ? 2 : 3;
-  for (int c = 0; c < tl.grid; ++c) {
-    int64_t load = 0;
-    for (int t = tl.cta_begin[c]; t < tl.cta_begin[c + 1]; ++t)
-      load += (int64_t)per_tile_units * (tl.tiles[t].kblocks + epi);
-    worst = std::max(worst, load);
-  }
-  return worst;
 }
 
 }  // namespace muon

@@ -116,6 +116,19 @@ std::string build_plan(const int64_t* shapes, const uint8_t* is_matrix, int32_t 
 TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_sms,
                     bool by_cost = true);
 
+// The tile lists of a persistent launch (all phases of all iterations in one launch, each
+// tile waiting until its matrix has finished the phase it reads): one list per
+// q = 3 * iteration + phase for q < 3 * iters, each with `units` entries in cta_begin.
+// The assignment follows a simulated run in cost units (k-blocks plus an epilogue
+// allowance per tile).  A tile is ready once every tile of its matrix's previous phase
+// (the previous iteration's Update, for a Gram tile) has finished, plus kPublishLag for
+// the stores to land; a phase's tiles, by readiness and then longest first, each go to
+// the unit that frees first, and each unit runs its tiles in that order.  The simulation
+// is causal, so the first lists do not depend on `iters`.
+std::vector<TileList> plan_persistent(const Plan& plan, int bm, int bn, int bk, int units,
+                                      int iters);
+constexpr int64_t kPublishLag = 2;
+
 // Owner of every matrix parameter for an n_shards-rank data-parallel group (one shard per
 // rank): longest Newton-Schulz cost first, each to the least-loaded rank among those that
 // hold a shard of it (ties: lowest rank).  owner[i] = -1 for non-matrix parameters;
@@ -142,9 +155,5 @@ struct XferRun {
 // of rank r's packed buffer.  Returns "" or a message (an owner out of range).
 std::string exchange_runs(const Plan& plan, const int32_t* owner, std::vector<XferRun>* runs,
                           std::vector<int64_t>* owner_offsets, std::vector<int64_t>* owned_numel);
-
-// Largest per-CTA load of a tile list, in the cost units plan_tiles balances
-// (k-blocks of 128 x 256 x 64 MMA work plus an epilogue allowance per tile).
-int64_t tile_makespan(const TileList& tl, int phase, int per_tile_units);
 
 }  // namespace muon
