@@ -255,6 +255,7 @@ struct EpiStage {
   uint8_t* dir;   // 2 KB, 512-byte aligned
   uint8_t* mir;   // 2 KB
   bool pending;   // a bulk store may still be reading these buffers (tracked by lane 0)
+  int groups;     // bulk-store groups committed for the current tile
 };
 
 __device__ __forceinline__ uint32_t swz64(int r, int c) {
@@ -359,6 +360,7 @@ __device__ __forceinline__ void epilogue_block(const NsParams& p, const MatDev& 
     bulk_commit();
   }
   st.pending = true;
+  ++st.groups;
 }
 
 // ---------------------------------------------------------------- plain-store epilogue
@@ -824,6 +826,8 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
     est.dir = tiles_smem + C::STAGES * C::STAGE_BYTES + (warp - 4) * 4096;
     est.mir = est.dir + 2048;
     est.pending = false;
+    est.groups = 0;
+    int prev_slot = -1;  // counter of the previous tile, not yet published
     for (int qq = p.q_begin; qq < p.q_end && !stop; ++qq) {
       const int it = qq / 3, phase = qq % 3;
       {
@@ -890,19 +894,33 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
             else mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[ab]), 0));
           }
           if (chained) {
-            // The tile's bulk stores must have landed before it is published.
-            if (est.pending) {
-              if (lane == 0) {
-                bulk_wait_all();
-                asm volatile("fence.proxy.async.global;" ::: "memory");
+            // A tile is published (its counter raised) once its bulk stores have landed.
+            // Inside a list that is done at the end of the next tile, whose own stores
+            // stay in flight meanwhile; the last tile of a list is published at once,
+            // since a later list of this CTA may wait on it.  Tiles of one list never
+            // wait on each other.
+            const bool last = ti + 1 >= bg[1];
+            if (last || prev_slot >= 0) {
+              if (est.pending) {
+                if (lane == 0) {
+                  if (last) bulk_wait_all();
+                  else bulk_wait_all_but(est.groups);
+                  asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
+                __syncwarp();
+                est.pending = !last;
               }
-              __syncwarp();
-              est.pending = false;
+              // All epilogue warps stop together, or publish together.  (Whether a tile
+              // publishes depends on its place in the list only: every warp agrees.)
+              stop = epi_any(!ok || *abort != 0);
+              if (stop) break;
+              if (warp == 4 && lane == 0) {
+                if (prev_slot >= 0) signal_counter(p.counters + prev_slot);
+                if (last) signal_counter(p.counters + tile.mat * 3 + phase);
+              }
             }
-            // All epilogue warps stop together, or publish the finished tile together.
-            stop = epi_any(!ok || *abort != 0);
-            if (stop) break;
-            if (warp == 4 && lane == 0) signal_counter(p.counters + tile.mat * 3 + phase);
+            prev_slot = last ? -1 : tile.mat * 3 + phase;
+            est.groups = 0;
           } else if (!ok) {
             stop = true;
             break;

@@ -255,15 +255,24 @@ std::vector<TileList> plan_persistent(const Plan& plan, int bm, int bn, int bk, 
       return ra != rb ? ra < rb : it[a].cost > it[b].cost;
     });
     std::vector<std::vector<TileDev>> per(units);
-    std::fill(done.begin(), done.end(), 0);
+    std::vector<std::vector<int64_t>> end(units);
     for (size_t k : order) {
       const Item& x = it[k];
       const Slot s = heap.top();
       heap.pop();
       const int64_t start = std::max(s.first, ready[x.t.mat]);
       per[s.second].push_back(x.t);
-      done[x.t.mat] = std::max(done[x.t.mat], start + x.cost + kPublishLag);
+      end[s.second].push_back(start + x.cost);
       heap.push({start + x.cost, s.second});
+    }
+    // A tile is published when the next tile of its list ends (the last one when it ends).
+    std::fill(done.begin(), done.end(), 0);
+    for (int u = 0; u < units; ++u) {
+      const size_t n = per[u].size();
+      for (size_t i = 0; i < n; ++i) {
+        const int64_t pub = end[u][i + 1 < n ? i + 1 : i] + kPublishLag;
+        done[per[u][i].mat] = std::max(done[per[u][i].mat], pub);
+      }
     }
     ready.swap(done);
     out.push_back(pack_lists(per, units));

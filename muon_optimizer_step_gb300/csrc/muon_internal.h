@@ -121,8 +121,10 @@ TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_s
 // q = 3 * iteration + phase for q < 3 * iters, each with `units` entries in cta_begin.
 // The assignment follows a simulated run in cost units (k-blocks plus an epilogue
 // allowance per tile).  A tile is ready once every tile of its matrix's previous phase
-// (the previous iteration's Update, for a Gram tile) has finished, plus kPublishLag for
-// the stores to land; a phase's tiles, by readiness and then longest first, each go to
+// (the previous iteration's Update, for a Gram tile) has been published: a tile is
+// published kPublishLag after the next tile of its list ends, or after itself ends when
+// it is the last of its list (the kernel's epilogue waits for a tile's stores at the end
+// of the next one).  A phase's tiles, by readiness and then longest first, each go to
 // the unit that frees first, and each unit runs its tiles in that order.  The simulation
 // is causal, so the first lists do not depend on `iters`.
 std::vector<TileList> plan_persistent(const Plan& plan, int bm, int bn, int bk, int units,
