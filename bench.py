@@ -66,10 +66,10 @@ def elementwise_bytes(n_matrix_elems, ns_dtype):
 # kernel shape and the sources it was taken with.
 NS_TRAFFIC = {
     # single-CTA tiles with the fused tail, as the 32-layer set runs (MUON_TC_KERNEL=1
-    # MUON_FUSED_TAIL=1 on two layers): 19.10 GB read + 8.90 GB written over 15 launches
-    "llama3_8b_x32": {"bytes_per_launch": 16 * (19103060480 + 8903074816) / 15,
+    # MUON_FUSED_TAIL=1 on two layers): 19.28 GB read + 8.90 GB written over 15 launches
+    "llama3_8b_x32": {"bytes_per_launch": 16 * (19282710528 + 8901469184) / 15,
                       "tile_shape": 1,
-                      "sources_sha256": "1c98d77418275fc9f7708f8944a1f3d7c48b4198b8109e0abe2cb029328f2946"},
+                      "sources_sha256": "cc05e20c8e85193f5defbb70b7c6ab32b78825e901fd7d86ef3f97815547cfee"},
 }
 NS_SOURCES = ("gemm_ns.cu", "device_common.cuh", "layout.cpp")
 
@@ -113,15 +113,16 @@ NS_KERNEL_NAMES = {
 }
 
 
-def ns_kernel_label(kernel, ns_steps, ns_dtype="bf16"):
+def ns_kernel_label(kernel, ns_steps, ns_dtype="bf16", fused=False):
     if kernel is None:
         return "ns_phase_f32_kernel (fp32 CUDA cores, 3 launches per iteration)"
     launches = 1 if kernel["persistent"] else 3 * ns_steps
     name = NS_KERNEL_NAMES[kernel["tile_shape"]] if ns_dtype == "bf16" else \
         "ns_tc_split_kernel (tcgen05 cta_group::2, fp32 as 3 bf16 parts, 6 products, " \
         "256x256 tiles)"
-    return "%s, %d units, %d launch(es) per step; the last Update also applies W" % (
-        name, kernel["units"], launches)
+    return "%s, %d units, %d launch(es) per step; %s" % (
+        name, kernel["units"], launches,
+        "the last Update also applies W" if fused else "a separate apply pass follows (timed apart)")
 
 
 # Process-group timeout of the multi-rank bench: far above any step, far below forever.
@@ -414,17 +415,32 @@ def run_ours(args):
     ws = capi.workspace_tensor(lay, dev)
     torch.cuda.synchronize()
 
-    # One timed step = the two calls muon_step makes (stage 1, then stages 2+3 with the
-    # apply fused into the last Newton-Schulz Update), with events between them.
+    # One timed step = the launches muon_step makes, through the public calls that split
+    # them into stages, with events between the stages: stage 1 (momentum and the
+    # Newton-Schulz input), then the Newton-Schulz launches, then the apply pass - or,
+    # where the library applies W inside the last Update, stages 2 and 3 as one call.
+    n_mat_elems = sum(r * c for (r, c), f in zip(wl.shapes, wl.is_matrix) if f)
+    fused = (ns_steps >= 1 and args.ns_dtype != "fp32" and n_mat_elems > 0
+             and capi.muon_layout_fused_apply(lay))
+
     def step_stages(evs=None):
         if evs is not None:
             evs[0].record()
         capi.muon_compute_momentum_inputs(G, M, lay, ws, wl.mu, wl.nesterov)
         if evs is not None:
             evs[1].record()
-        capi.muon_orthogonalize_apply(W, lay, ws, wl.lr, wl.wd, ns_steps)
-        if evs is not None:
-            evs[2].record()
+        if fused:
+            capi.muon_orthogonalize_apply(W, lay, ws, wl.lr, wl.wd, ns_steps)
+            if evs is not None:
+                evs[2].record()
+                evs[3].record()
+        else:
+            capi.muon_orthogonalize_updates(lay, ws, ns_steps)
+            if evs is not None:
+                evs[2].record()
+            capi.muon_apply_local_updates(W, lay, ws, wl.lr, wl.wd, ns_steps)
+            if evs is not None:
+                evs[3].record()
 
     for _ in range(args.warmup):
         step_stages()
@@ -434,7 +450,7 @@ def run_ours(args):
         if dist is not None:
             dist.barrier()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -452,9 +468,9 @@ def run_ours(args):
     barrier()
     capi.muon_check()
     total_ms = t_start.elapsed_time(t_end)
-    stage_ms = [0.0, 0.0]
+    stage_ms = [0.0, 0.0, 0.0]
     for e in evs:
-        for j in range(2):
+        for j in range(3):
             stage_ms[j] += e[j].elapsed_time(e[j + 1])
     stage_ms = [x / args.steps for x in stage_ms]
     red = reduce_max_over_ranks([total_ms] + stage_ms, dist, dev)
@@ -547,9 +563,7 @@ def run_ours(args):
 
     peaks = load_peaks()
     sym, dense = ns_flops(wl.shapes, wl.is_matrix, ns_steps)
-    n_mat_elems = sum(r * c for (r, c), f in zip(wl.shapes, wl.is_matrix) if f)
     b1, b3 = elementwise_bytes(n_mat_elems, args.ns_dtype)
-    fused_tail = args.ns_dtype != "fp32" and ns_steps >= 1
     ns_ms = stage_ms[1]
     ns_tflops = sym / (ns_ms * 1e-3) / 1e12
     ew_ms = stage_ms[0]
@@ -572,7 +586,7 @@ def run_ours(args):
         if ns_steps >= 1 else 0
     # stage 1 (momentum + norm finalize), the Newton-Schulz launches, and the apply pass
     # unless the last Update applies W
-    launches_per_step = (2 + ns_launches + (0 if fused_tail else 1)) if n_mat_elems else 0
+    launches_per_step = (2 + ns_launches + (0 if fused else 1)) if n_mat_elems else 0
     line = {
         "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
@@ -588,10 +602,13 @@ def run_ours(args):
         "ns_flops_sym": sym,
         # whole job: every rank steps its own replica in the (max over ranks) step time
         "matrices_per_s": world * wl.n_matrices / (ms * 1e-3),
-        "stage_ms": {"momentum_inputs": stage_ms[0], "orthogonalize_apply": stage_ms[1]},
-        "fused_apply": fused_tail,
+        "stage_ms": ({"momentum_inputs": stage_ms[0], "orthogonalize_apply": stage_ms[1]}
+                     if fused else
+                     {"momentum_inputs": stage_ms[0], "newton_schulz": stage_ms[1],
+                      "apply": stage_ms[2]}),
+        "fused_apply": bool(fused),
         "roofline": {"bound": "alu" if args.ns_dtype == "fp32" else "tensor",
-                     "kernel": ns_kernel_label(ns_kernel, ns_steps, args.ns_dtype),
+                     "kernel": ns_kernel_label(ns_kernel, ns_steps, args.ns_dtype, fused),
                      "achieved": ns_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": ns_tflops / peak_tc,
                      "frac_of_burst": (ns_tflops / peaks["bf16_tflops"]
@@ -606,6 +623,12 @@ def run_ours(args):
                                  "achieved": ew_gbs, "peak": peaks["hbm_gbs"],
                                  "unit": "GB/s", "frac": ew_gbs / peaks["hbm_gbs"],
                                  "bytes_per_step": b1},
+        "roofline_apply": (None if fused else
+                           {"bound": "hbm", "kernel": "apply_kernel",
+                            "achieved": b3 / (stage_ms[2] * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                            "unit": "GB/s",
+                            "frac": b3 / (stage_ms[2] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                            "bytes_per_step": b3}),
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "e2e": e2e,

@@ -304,6 +304,16 @@ int32_t muon_abi_version(void);
  * environment (MUON_TC_KERNEL) pins a shape the device cannot run. */
 muon_status muon_layout_ns_kernel(const muon_layout* layout, int32_t* tile_shape, int32_t* units,
                                   int32_t* persistent);
+/* Where muon_step, muon_step_grouped and muon_orthogonalize_apply apply the update to W
+ * on the current device: *fused = 1 inside the last Newton-Schulz Update's epilogue (from
+ * the fp32 O), 0 in a separate streaming pass after the last Update (the pass
+ * muon_apply_local_updates runs).  Prepares the layout's device tables first, as
+ * muon_layout_ns_kernel does.  Tensor-core layouts fuse when one iteration carries
+ * >= 20 TFLOP (symmetric count, sum over matrices of 3 m^2 n + m^3); the environment
+ * variable MUON_FUSED_TAIL=0 or 1 pins the choice for layouts prepared afterwards.  fp32
+ * layouts and layouts without matrices report 0, and a call with ns_steps = 0 never fuses.
+ * The pages have no counterpart: a choice this library makes, reported for measurements. */
+muon_status muon_layout_fused_apply(const muon_layout* layout, int32_t* fused);
 /* Self-test of the bounded-wait path: launches one block that waits on an mbarrier nobody
  * arrives on, with a budget of budget_cycles clock cycles (1..2^40).  The wait runs out,
  * the kernel records MUON_ERR_TIMEOUT and returns; a following muon_check reports it. */

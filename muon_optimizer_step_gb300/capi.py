@@ -80,6 +80,7 @@ SIGNATURES = [
     ("muon_selftest_device_check", _I32, [_P]),
     ("muon_layout_ns_kernel", _I32, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32),
                                      ctypes.POINTER(_I32)]),
+    ("muon_layout_fused_apply", _I32, [_P, ctypes.POINTER(_I32)]),
 ]
 
 
@@ -379,6 +380,14 @@ def muon_layout_ns_kernel(layout) -> dict:
                                      ctypes.byref(pers)), "muon_layout_ns_kernel")
     return {"tile_shape": int(shape.value), "units": int(units.value),
             "persistent": bool(pers.value)}
+
+
+def muon_layout_fused_apply(layout) -> bool:
+    """True when muon_step / muon_orthogonalize_apply apply the update to W inside the last
+    Newton-Schulz Update on the current device, False when a separate apply pass runs."""
+    f = _I32()
+    _check(lib.muon_layout_fused_apply(layout.handle, ctypes.byref(f)), "muon_layout_fused_apply")
+    return bool(f.value)
 
 
 def muon_last_error() -> str:

@@ -777,6 +777,16 @@ muon_status muon_layout_ns_kernel(const muon_layout* layout, int32_t* tile_shape
   return ok();
 }
 
+muon_status muon_layout_fused_apply(const muon_layout* layout, int32_t* fused) {
+  if (layout == nullptr || fused == nullptr) return fail(MUON_ERR_INVALID_ARG, "null argument");
+  muon_layout* L = const_cast<muon_layout*>(layout);
+  std::lock_guard<std::mutex> guard(L->mu);
+  MUON_TRY(ensure_device(L));
+  const bool tc = L->plan.ns_dtype != MUON_NS_FP32 && !L->plan.mats.empty();
+  *fused = tc && L->dt.fused_tail ? 1 : 0;
+  return ok();
+}
+
 int32_t muon_debug_build(void) { return kDebugChecks ? 1 : 0; }
 
 muon_status muon_selftest_device_check(cudaStream_t stream) {

@@ -499,24 +499,35 @@ def test_default_kernel_choice(capi, monkeypatch):
     """256 x 512 CTA-pair tiles for two Llama-3-8B layers (long reductions); CTA pairs for
     the GPT-2-small and MoE sets; single CTAs for the 32-layer set (94 TFLOP per
     iteration: long enough to run at the power limit); one launch per phase, except
-    GPT-2-small (0.22 TFLOP per iteration: one persistent launch); nothing on the fp32
-    path; an unknown pin is an error."""
+    GPT-2-small (0.22 TFLOP per iteration: one persistent launch); the update applied to W
+    inside the last Update on the 32-layer set only (the others run the apply pass);
+    nothing on the fp32 path; an unknown pin is an error."""
     monkeypatch.delenv("MUON_TC_KERNEL", raising=False)
     monkeypatch.delenv("MUON_NS_PERSISTENT", raising=False)
+    monkeypatch.delenv("MUON_FUSED_TAIL", raising=False)
 
     def choice(name, dtype=0):
         wl = inputs.WORKLOADS[name]
-        return capi.muon_layout_ns_kernel(capi.muon_layout_create(wl.shapes, 1, dtype,
-                                                                  wl.is_matrix))
+        lay = capi.muon_layout_create(wl.shapes, 1, dtype, wl.is_matrix)
+        k = capi.muon_layout_ns_kernel(lay)
+        k["fused"] = capi.muon_layout_fused_apply(lay)
+        return k
     k = choice("llama3_8b_x2")
     assert k["tile_shape"] == 3 and not k["persistent"] and k["units"] >= 1, k
+    assert not k["fused"], k
     k = choice("llama3_8b_x32")
     assert k["tile_shape"] == 1 and not k["persistent"] and k["units"] >= 1, k
+    assert k["fused"], k
     k = choice("gpt2_small_x12")
     assert k["tile_shape"] == 2 and k["persistent"] and k["units"] >= 1, k
+    assert not k["fused"], k
     k = choice("moe_64e")
     assert k["tile_shape"] == 2 and not k["persistent"] and k["units"] >= 1, k
-    assert choice("gpt2_small_x12", 1) == {"tile_shape": 0, "units": 0, "persistent": False}
+    assert not k["fused"], k
+    assert choice("gpt2_small_x12", 1) == {"tile_shape": 0, "units": 0, "persistent": False,
+                                           "fused": False}
+    monkeypatch.setenv("MUON_FUSED_TAIL", "1")
+    assert choice("gpt2_small_x12")["fused"]
     monkeypatch.setenv("MUON_TC_KERNEL", "4")
     with pytest.raises(capi.MuonError) as e:
         choice("llama3_8b_x2")
