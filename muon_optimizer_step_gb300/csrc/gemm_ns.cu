@@ -180,6 +180,15 @@ __device__ __forceinline__ TileOps tile_ops(const MatDev& mt, int phase, int x_i
   return o;
 }
 
+// A 256-column tile whose second 128 columns lie past the matrix computes its first 128
+// only (N = 128 MMAs).  On a CTA pair each CTA then holds 64 rows of B (the pair's MMA
+// takes N/2 of B from each CTA), so its B rows start 64, not 128, after the tile's.
+template <bool kNarrowable>
+__device__ __forceinline__ bool narrow_tile(const MatDev& mt, const TileDev& tile, int phase) {
+  const int n_out = phase == kPhaseUpdate ? mt.cols : mt.m;
+  return kNarrowable && tile.j0 + 128 >= n_out;
+}
+
 // The counter a tile of (it, phase) waits on, and the value that means "complete".
 __device__ __forceinline__ int dep_slot(const MatDev& mt, int mat, int it, int phase,
                                         int* target) {
@@ -628,7 +637,8 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
             const CUtensorMap* amap = p.tmaps + (size_t)tile.mat * kMapsPerMat + ops.a_map;
             const CUtensorMap* bmap = p.tmaps + (size_t)tile.mat * kMapsPerMat + ops.b_map;
             const int ia = tile.i0 + (kCluster ? 128 * (int)rank : 0);
-            const int jr = tile.j0 + (kCluster ? 128 * (int)rank : 0);
+            const bool narrow = narrow_tile<!C::kWide>(mt, tile, phase);
+            const int jr = tile.j0 + (kCluster ? (narrow ? 64 : 128) * (int)rank : 0);
             for (int kb = 0; kb < tile.kblocks; ++kb) {
               if (!wait_role<kCluster>(&empty[stage], ph ^ 1u, p, abort, peer_abort)) {
                 ok = false;
@@ -717,18 +727,20 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
             const TileDev tile = p.tiles[ti];
             const MatDev& mt = p.mats[tile.mat];
             const TileOps ops = tile_ops<kCluster>(mt, phase, it & 1);
-            // Columns the epilogue would discard are not computed (single CTAs; a pair's
-            // MMA covers both CTAs' rows, so it cannot skip per CTA):
-            //  - symmetric phases: a tile whose rows all lie at or below its second column
-            //    half (i0 = j0 + 128) skips the first half;
-            //  - a tile whose second column half lies outside the matrix skips that half.
+            // Columns the epilogue would discard are not computed:
+            //  - symmetric phases, single CTAs: a tile whose rows all lie at or below its
+            //    second column half (i0 = j0 + 128) skips the first half (a pair's MMA
+            //    covers both CTAs' rows, so it cannot skip per CTA);
+            //  - a 256-column tile whose second column half lies outside the matrix skips
+            //    that half (narrow_tile; on a pair the producer has placed each CTA's 64
+            //    rows of the first half).
             // A half is done as N = 128 MMAs on that half of B, into that half of the
             // accumulator.
             const int row0 = tile.i0 + (kCluster ? 128 * (int)rank : 0);
             const int n_out = phase == kPhaseUpdate ? mt.cols : mt.m;
             const int m_out = phase == kPhaseUpdate ? mt.rows : mt.m;
             const bool skip_first = !kTwoSm && phase != kPhaseUpdate && tile.j0 + 128 <= row0;
-            const bool skip_second = !kTwoSm && tile.j0 + 128 >= n_out;
+            const bool skip_second = narrow_tile<!C::kWide>(mt, tile, phase);
             const bool idle = !kTwoSm && (row0 >= m_out || (skip_first && skip_second));
             const bool half_n = !idle && (skip_first || skip_second);
             const uint32_t idesc = idesc_bf16(C::MMA_M, half_n ? BN / 2 : BN, ops.a_mn, ops.b_mn);
