@@ -379,6 +379,7 @@ muon_status run_ns_apply(muon_layout* L, const ShardPtrs& w, void* ws, const Gro
     ApplyArgs ap;
     ap.W = w;
     ap.L = L->plan.L;
+    ap.inv_L = 1.0f / (float)L->plan.L;
     ap.gp = gp;
     return run_ns(L, ws, ns_steps, &ap, st);
   }

@@ -445,8 +445,25 @@ struct GroupParams {
 struct ApplyArgs {
   ShardPtrs W;     // parameter shards
   long long L;     // shard length
+  float inv_L;     // 1 / L, rounded to fp32 (shard_of's estimate)
   GroupParams gp;  // lr and decay per group
 };
+
+// Shard and in-shard offset of flat element g (0 <= g < n_shards * L), without a 64-bit
+// division: the fp32 estimate of g / L (< 2^7) is off by at most one, and is corrected.
+__device__ __forceinline__ long long shard_of(const ApplyArgs& ap, long long g, long long* off) {
+  long long s = (long long)((float)g * ap.inv_L);
+  long long o = g - s * ap.L;
+  if (o < 0) {
+    --s;
+    o += ap.L;
+  } else if (o >= ap.L) {
+    ++s;
+    o -= ap.L;
+  }
+  *off = o;
+  return s;
+}
 
 // Debug builds: the shards a matrix's apply writes exist.
 __device__ __forceinline__ bool debug_apply_ok(const ApplyArgs& ap, const MatDev& mt,
@@ -463,8 +480,8 @@ __device__ __forceinline__ void apply_row_run(const ApplyArgs& ap, const MatDev&
   const float lrs = ap.gp.lr[mt.group] * mt.scale;
   const float decay = ap.gp.decay[mt.group];
   const long long g0 = mt.flat_off + (long long)i * mt.cols + jb;
-  const long long s0 = g0 / ap.L;
-  const long long off0 = g0 - s0 * ap.L;
+  long long off0;
+  const long long s0 = shard_of(ap, g0, &off0);
   if (n == 32 && off0 + 32 <= ap.L && (off0 & 3) == 0) {
     float4* w = reinterpret_cast<float4*>(ap.W.p[s0] + off0);
 #pragma unroll
@@ -480,9 +497,9 @@ __device__ __forceinline__ void apply_row_run(const ApplyArgs& ap, const MatDev&
 #pragma unroll
     for (int t = 0; t < 32; ++t) {
       if (t < n) {
-        const long long g = g0 + t;
-        const long long s = g / ap.L;
-        float* w = ap.W.p[s] + (g - s * ap.L);
+        long long off;
+        const long long s = shard_of(ap, g0 + t, &off);
+        float* w = ap.W.p[s] + off;
         *w = fmaf(-lrs, o[t], *w * decay);
       }
     }
@@ -494,8 +511,8 @@ __device__ __forceinline__ void apply_row_run(const ApplyArgs& ap, const MatDev&
 __device__ __forceinline__ bool apply_load_row_run(const ApplyArgs& ap, const MatDev& mt, int i,
                                                    int jb, float (&w)[32]) {
   const long long g0 = mt.flat_off + (long long)i * mt.cols + jb;
-  const long long s0 = g0 / ap.L;
-  const long long off0 = g0 - s0 * ap.L;
+  long long off0;
+  const long long s0 = shard_of(ap, g0, &off0);
   if (off0 + 32 <= ap.L && (off0 & 3) == 0) {
     // Weights are touched once per step: stream them past L2 (evict first) so they do
     // not push out the X and B panels the tile wave is reusing.
@@ -520,8 +537,9 @@ __device__ __forceinline__ void apply_store_row_run(const ApplyArgs& ap, const M
   const float lrs = ap.gp.lr[mt.group] * mt.scale;
   const float decay = ap.gp.decay[mt.group];
   const long long g0 = mt.flat_off + (long long)i * mt.cols + jb;
-  const long long s0 = g0 / ap.L;
-  float4* dst = reinterpret_cast<float4*>(ap.W.p[s0] + (g0 - s0 * ap.L));
+  long long off0;
+  const long long s0 = shard_of(ap, g0, &off0);
+  float4* dst = reinterpret_cast<float4*>(ap.W.p[s0] + off0);
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     float4 v;
