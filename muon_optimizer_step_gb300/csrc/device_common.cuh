@@ -506,6 +506,87 @@ __device__ __forceinline__ void apply_row_run(const ApplyArgs& ap, const MatDev&
   }
 }
 
+// Asks L2 to fetch n weights of matrix row i from column jb: one bulk prefetch when the
+// run lies in one shard and starts on a 16-byte boundary (shard bases are 16-byte
+// aligned), nothing otherwise.  A hint: no data reaches the SM and nothing waits on it.
+__device__ __forceinline__ void prefetch_w_row(const ApplyArgs& ap, const MatDev& mt, int i,
+                                               int jb, int n) {
+  if (i >= mt.rows || jb >= mt.cols) return;
+  n = min(n, mt.cols - jb);
+  const long long g0 = mt.flat_off + (long long)i * mt.cols + jb;
+  long long off;
+  const long long s = shard_of(ap, g0, &off);
+  const uint32_t bytes = (uint32_t)(4 * n) & ~15u;
+  if (bytes == 0 || off + n > ap.L || (off & 3) != 0) return;
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ap.W.p[s] + off), "r"(bytes)
+               : "memory");
+}
+
+// W <- W*decay - lr*scale*O on the 32 x 32 block of matrix mt at rows r0.., columns jb..,
+// whose fp32 O the warp holds one row per lane (o = row r0 + lane).  The lanes' rows are
+// 4 KB apart in W, so the block is first turned around in `scratch` (4 KB of shared
+// memory, 16-byte aligned, not read by any pending bulk store): 16-byte chunk k of row r
+// goes to slot 8r + (k ^ (r & 7)), which keeps both passes free of bank conflicts.  Each
+// weight access then covers four whole rows (8 lanes x 16 bytes per row), and the eight
+// loads of a lane are all issued before the first store.  Chunks past the matrix are
+// skipped; a chunk that leaves its shard or a 16-byte boundary goes element by element.
+__device__ __forceinline__ void apply_block(const ApplyArgs& ap, const MatDev& mt, int r0, int jb,
+                                            int lane, const float (&o)[32], uint8_t* scratch) {
+  float4* sc = reinterpret_cast<float4*>(scratch);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    sc[8 * lane + (k ^ (lane & 7))] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+  __syncwarp();
+  const float lrs = ap.gp.lr[mt.group] * mt.scale;
+  const float decay = ap.gp.decay[mt.group];
+  const int cc = lane & 7;                 // this lane's 16-byte chunk of a row
+  const int col = jb + 4 * cc;
+  float4 w[8];
+  float* wp[8];
+  bool vec[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int rr = 4 * j + (lane >> 3);    // block row of access j
+    const int row = r0 + rr;
+    wp[j] = nullptr;
+    vec[j] = false;
+    if (row < mt.rows && col < mt.cols) {
+      long long off;
+      const long long g = mt.flat_off + (long long)row * mt.cols + col;
+      const long long sh = shard_of(ap, g, &off);
+      wp[j] = ap.W.p[sh] + off;
+      vec[j] = col + 4 <= mt.cols && off + 4 <= ap.L && (off & 3) == 0;
+      if (vec[j]) w[j] = __ldcs(reinterpret_cast<const float4*>(wp[j]));
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (wp[j] == nullptr) continue;
+    const int rr = 4 * j + (lane >> 3);
+    const float4 ov = sc[8 * rr + (cc ^ (rr & 7))];
+    if (vec[j]) {
+      float4 v = w[j];
+      v.x = fmaf(-lrs, ov.x, v.x * decay);
+      v.y = fmaf(-lrs, ov.y, v.y * decay);
+      v.z = fmaf(-lrs, ov.z, v.z * decay);
+      v.w = fmaf(-lrs, ov.w, v.w * decay);
+      __stcs(reinterpret_cast<float4*>(wp[j]), v);
+    } else {
+      const float oe[4] = {ov.x, ov.y, ov.z, ov.w};
+      const long long g = mt.flat_off + (long long)(r0 + rr) * mt.cols + col;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (col + e >= mt.cols) break;
+        long long off;
+        const long long sh = shard_of(ap, g + e, &off);
+        float* x = ap.W.p[sh] + off;
+        *x = fmaf(-lrs, oe[e], *x * decay);
+      }
+    }
+  }
+  __syncwarp();  // every lane is done with the scratch
+}
+
 // Two-part form of apply_row_run for a full run of 32: load the weights first (returns
 // whether the 128-bit path applies), store them updated later.
 __device__ __forceinline__ bool apply_load_row_run(const ApplyArgs& ap, const MatDev& mt, int i,

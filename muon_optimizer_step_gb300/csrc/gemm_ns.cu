@@ -288,18 +288,16 @@ __device__ __forceinline__ void epilogue_block(const NsParams& p, const MatDev& 
   bool mirror = false;
   if (phase == kPhaseUpdate) {
     if (r0 >= mt.rows || jb >= mt.cols) return;  // warp-uniform
-    if (apply && i < mt.rows) {
-      // Issue the weight loads before any store so that the round trips overlap.
-      float w[32];
-      const int n = min(32, mt.cols - jb);
-      const bool vec = n == 32 && apply_load_row_run(p.ap, mt, i, jb, w);
 #pragma unroll
-      for (int t = 0; t < 32; ++t) f[t] = s * __uint_as_float(acc[t]);
-      if (vec) apply_store_row_run(p.ap, mt, i, jb, true, w, f);
-      else apply_row_run(p.ap, mt, i, jb, n, f);
-    } else {
-#pragma unroll
-      for (int t = 0; t < 32; ++t) f[t] = s * __uint_as_float(acc[t]);
+    for (int t = 0; t < 32; ++t) f[t] = s * __uint_as_float(acc[t]);
+    if (apply) {
+      // The staging buffers (4 KB) turn the block around for coalesced weight accesses,
+      // once the previous bulk store has read them.
+      if (st.pending) {
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+      }
+      apply_block(p.ap, mt, r0, jb, lane, f, st.dir);
     }
     out_map = maps + (x_in ? kMapX0St : kMapX1St);
   } else {
@@ -851,6 +849,11 @@ __device__ __forceinline__ void ns_tc_body(const NsParams& p) {
           const MatDev& mt = p.mats[tile.mat];
           const int ab = lt % C::ACC_BUFS;
           const uint32_t use = (uint32_t)(lt / C::ACC_BUFS);
+          // Applying Update: while this tile's MMAs run, each lane asks L2 for the weights
+          // of its row and this warp's columns, so that the epilogue's loads hit L2.
+          if (apply)
+            prefetch_w_row(p.ap, mt, tile.i0 + (kCluster ? 128 * (int)rank : 0) + 32 * q + lane,
+                           tile.j0 + half * (C::TILE_N / 2), C::TILE_N / 2);
           bool ok = *abort == 0 && mbar_wait_bounded(&acc_full[ab], use & 1u, p.budget, p.err,
                                                      abort);
           ok = __all_sync(0xffffffffu, ok);
