@@ -587,51 +587,6 @@ __device__ __forceinline__ void apply_block(const ApplyArgs& ap, const MatDev& m
   __syncwarp();  // every lane is done with the scratch
 }
 
-// Two-part form of apply_row_run for a full run of 32: load the weights first (returns
-// whether the 128-bit path applies), store them updated later.
-__device__ __forceinline__ bool apply_load_row_run(const ApplyArgs& ap, const MatDev& mt, int i,
-                                                   int jb, float (&w)[32]) {
-  const long long g0 = mt.flat_off + (long long)i * mt.cols + jb;
-  long long off0;
-  const long long s0 = shard_of(ap, g0, &off0);
-  if (off0 + 32 <= ap.L && (off0 & 3) == 0) {
-    // Weights are touched once per step: stream them past L2 (evict first) so they do
-    // not push out the X and B panels the tile wave is reusing.
-    const float4* src = reinterpret_cast<const float4*>(ap.W.p[s0] + off0);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float4 v = __ldcs(src + q);
-      w[4 * q + 0] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
-    }
-    return true;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void apply_store_row_run(const ApplyArgs& ap, const MatDev& mt, int i,
-                                                    int jb, bool vec, const float (&w)[32],
-                                                    const float (&o)[32]) {
-  if (!vec) {
-    apply_row_run(ap, mt, i, jb, 32, o);
-    return;
-  }
-  const float lrs = ap.gp.lr[mt.group] * mt.scale;
-  const float decay = ap.gp.decay[mt.group];
-  const long long g0 = mt.flat_off + (long long)i * mt.cols + jb;
-  long long off0;
-  const long long s0 = shard_of(ap, g0, &off0);
-  float4* dst = reinterpret_cast<float4*>(ap.W.p[s0] + off0);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    float4 v;
-    v.x = fmaf(-lrs, o[4 * q + 0], w[4 * q + 0] * decay);
-    v.y = fmaf(-lrs, o[4 * q + 1], w[4 * q + 1] * decay);
-    v.z = fmaf(-lrs, o[4 * q + 2], w[4 * q + 2] * decay);
-    v.w = fmaf(-lrs, o[4 * q + 3], w[4 * q + 3] * decay);
-    __stcs(dst + q, v);
-  }
-}
-
 // ------------------------------------------------------------------ small math helpers
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
