@@ -205,8 +205,9 @@ muon_status ensure_device(muon_layout* L) {
     // One launch per phase, each phase's tiles balanced on their own, except for tiny
     // buffers: there fixed costs per launch weigh most, and the persistent launch (every
     // phase in one launch, tiles waiting on per-matrix counters) measured faster on
-    // GPT-2-small with CTA pairs (1.487 against 1.572 ms per step) but slower on MoE
-    // (15.7 against 14.8 ms) and two Llama layers (22.9 against 20.1 ms).  The split-fp32
+    // GPT-2-small with CTA pairs (1.487 against 1.572 ms per step, before its tile lists
+    // were planned from a simulated run; 1.409 after) but slower on MoE (15.4 against
+    // 14.8 ms) and two Llama layers (20.9 against 19.2 ms), planned lists included.  The split-fp32
     // epilogue writes with plain stores, which the persistent launch's counters do not
     // publish to the next phase's TMA reads, so it never runs persistent.
     t.tc_persistent = !split && all < kPersistentFlops;
