@@ -423,6 +423,35 @@ def test_each_tcgen05_variant_vs_oracle(capi, variant, persistent, monkeypatch):
                         (variant, persistent, wl.shapes[i]))
 
 
+@pytest.mark.parametrize("variant", ["1", "2", "3"])
+def test_persistent_lists_past_the_planned_iterations(capi, variant, monkeypatch):
+    """A persistent launch plans tile lists for six iterations and reuses the sixth's for
+    later ones.  Each tile computes the same bits whichever list holds it, so the
+    persistent launch must equal one launch per phase bit for bit, here at 8 iterations
+    (and at 6 and 1, the planned and the shortest case)."""
+    monkeypatch.setenv("MUON_TC_KERNEL", variant)
+    shapes = [(300, 200), (130, 520), (7, 3), (64, 1000), (257, 129), (600, 1100), (1100, 600),
+              (768, 768), (768, 2304)]
+    wl = inputs.Workload("mixed_long", tuple(shapes), (True,) * len(shapes), 1, seed=12, rank=4)
+    X = recipe_inputs(wl, 4)
+    lays = {}
+    for pers in ("1", "0"):
+        monkeypatch.setenv("MUON_NS_PERSISTENT", pers)
+        lay = capi.muon_layout_create(wl.shapes, 1, 0, wl.is_matrix)
+        assert capi.muon_layout_ns_kernel(lay)["persistent"] == (pers == "1")
+        lays[pers] = lay
+    for ns_steps in (8, 6, 1):
+        outs = {}
+        for pers, lay in lays.items():
+            ws = capi.workspace_tensor(lay)
+            out = torch.zeros(lay.full_numel, device="cuda")
+            capi.muon_orthogonalize_full(lay, ws, mats_to_full(X, lay), out, ns_steps)
+            capi.muon_check()
+            outs[pers] = out.cpu()
+        assert torch.equal(outs["1"], outs["0"]), (variant, ns_steps)
+        assert torch.isfinite(outs["1"]).all()
+
+
 GROUP_HP = [(0.02, 0.01, 0.95, True), (0.05, 0.0, 0.9, False), (0.001, 0.1, 0.5, True)]
 
 
