@@ -111,8 +111,8 @@ std::string build_plan(const int64_t* shapes, const uint8_t* is_matrix, int32_t 
                        int32_t n_shards, int32_t ns_dtype, Plan* plan);
 
 // Assignment of a phase's tiles to `grid` CTAs (grid <= n_sms), each tile to the least
-// loaded CTA: longest first (by_cost), or in matrix order (so that, in a persistent launch,
-// matrices finish a phase one after another and their next phase can start early).
+// loaded CTA: longest first (by_cost), or in matrix order.  One launch per phase uses the
+// first; a persistent launch plans its lists with plan_persistent instead.
 TileList plan_tiles(const Plan& plan, int phase, int bm, int bn, int bk, int n_sms,
                     bool by_cost = true);
 
